@@ -1,0 +1,518 @@
+// Host runtime of the CLO decode-step library: the C ABI declared in clo.h.
+//
+// One context owns a pinned, device-mapped host pool holding every sequence's
+// full K/V (CLO keeps the whole KV cache in CPU memory: CLO abstract) and the HBM
+// state of the decode step.  clo_decode_step() only enqueues kernels on the
+// context's stream; no host synchronisation happens between layers or phases
+// (GPU-centric synchronisation: CLO abstract, feature (3)).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "clo.h"
+#include "clo_internal.cuh"
+
+using namespace clo;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+clo_status fail(clo_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+#define CLO_CUDA(expr)                                                                         \
+  do {                                                                                         \
+    cudaError_t e_ = (expr);                                                                   \
+    if (e_ != cudaSuccess) return fail(CLO_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+constexpr int kSplitRows = 256;
+constexpr int64_t kSelTargetChunk = 16384;
+constexpr int64_t kSelTile = 512;
+constexpr int64_t kStageTokens = 16384;
+
+int64_t topk_for(int64_t N, int64_t topk, double ratio) {
+  if (N <= 0) return 0;
+  if (topk > 0) return std::min<int64_t>(topk, N);
+  int64_t k = (int64_t)std::ceil(ratio * (double)N);
+  return std::max<int64_t>(1, std::min<int64_t>(k, N));
+}
+
+}  // namespace
+
+struct clo_ctx {
+  clo_config cfg{};
+  int L = 0, B = 0, Hq = 0, Hkv = 0, d = 0, G = 0, P = 0;
+  int64_t Nmax = 0, kmax = 0, U = 0;
+  cudaStream_t stream = nullptr;
+  uint16_t* pool_host = nullptr;
+  DevState ds{};
+  std::vector<void*> dev_allocs;
+  std::vector<int64_t> ntok;  // [L*B] tokens appended per (layer, seq)
+  bool ntok_dirty = true;
+  int64_t* ntok_pinned = nullptr;  // [B] + k [B] staging for uploads
+  int64_t step = 0;
+  bool warmup_mode = false;
+  int W = 0;
+  bool warmup_done = false;
+  int sel_cluster = 1;
+  int64_t sel_chunk = 0;
+  uint16_t* kstage = nullptr;
+  uint16_t* vstage = nullptr;
+  uint16_t* q_io = nullptr;
+  float* out_io = nullptr;
+  cudaEvent_t ev[5] = {};
+  bool have_events = false;
+  bool step_timed = false;
+  uint32_t epoch = 0;
+  std::vector<uint8_t> persist_host;  // valid once known
+  bool persist_host_valid = false;
+
+  template <class T>
+  clo_status dalloc(T** p, size_t count) {
+    void* v = nullptr;
+    const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+    cudaError_t e = cudaMalloc(&v, bytes);
+    if (e != cudaSuccess) return fail(CLO_ERR_OOM, "cudaMalloc(" + std::to_string(bytes) + "): " + cudaGetErrorString(e));
+    dev_allocs.push_back(v);
+    e = cudaMemset(v, 0, bytes);
+    if (e != cudaSuccess) return fail(CLO_ERR_CUDA, std::string("cudaMemset: ") + cudaGetErrorString(e));
+    *p = static_cast<T*>(v);
+    return CLO_OK;
+  }
+
+  void release() {
+    if (stream) cudaStreamSynchronize(stream);
+    for (void* p : dev_allocs) cudaFree(p);
+    dev_allocs.clear();
+    if (pool_host) cudaFreeHost(pool_host);
+    pool_host = nullptr;
+    if (ntok_pinned) cudaFreeHost(ntok_pinned);
+    ntok_pinned = nullptr;
+    if (have_events)
+      for (auto& e : ev) cudaEventDestroy(e);
+    have_events = false;
+  }
+};
+
+#define CLO_TRY(expr)                 \
+  do {                                \
+    clo_status s_ = (expr);           \
+    if (s_ != CLO_OK) return s_;      \
+  } while (0)
+
+extern "C" {
+
+CLO_API void clo_config_default(clo_config* cfg) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof(*cfg));
+  cfg->topk_ratio = 0.1;
+  cfg->warmup_steps = 16;
+  cfg->tau_offset = 0.05f;
+  cfg->wait_timeout_ns = 2000000000LL;
+  cfg->debug_drop_flag_layer = -1;
+}
+
+CLO_API const char* clo_last_error(void) { return g_last_error.c_str(); }
+
+static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
+  c->cfg = *cfg;
+  c->L = cfg->n_layers;
+  c->B = cfg->batch;
+  c->Hq = cfg->n_q_heads;
+  c->Hkv = cfg->n_kv_heads;
+  c->d = cfg->head_dim;
+  if (c->L < 1 || c->B < 1 || c->Hkv < 1 || c->Hq < 1 || c->Hq % c->Hkv != 0)
+    return fail(CLO_ERR_INVALID, "shapes: need L, B, Hkv >= 1 and Hq a multiple of Hkv");
+  c->G = c->Hq / c->Hkv;
+  if (c->G > kMaxG) return fail(CLO_ERR_INVALID, "GQA group Hq/Hkv must be <= 8");
+  if (c->d != 64 && c->d != 128) return fail(CLO_ERR_INVALID, "head_dim must be 64 or 128");
+  if (cfg->max_tokens < 1 || cfg->max_tokens > kMaxTokens)
+    return fail(CLO_ERR_INVALID, "max_tokens must be in [1, 524288]");
+  if (!cfg->hash_R) return fail(CLO_ERR_INVALID, "hash_R (bf16 [L][Hkv][d][128]) is required");
+  if (cfg->topk < 0) return fail(CLO_ERR_INVALID, "topk must be >= 0");
+  if (cfg->topk == 0 && !(cfg->topk_ratio > 0.0 && cfg->topk_ratio <= 1.0))
+    return fail(CLO_ERR_INVALID, "topk_ratio must be in (0, 1] when topk == 0");
+  c->warmup_mode = cfg->tau == nullptr;
+  if (c->warmup_mode) {
+    if (cfg->warmup_steps < 2) return fail(CLO_ERR_INVALID, "warmup_steps must be >= 2 when tau is NULL");
+    if (cfg->n_persist < 0 || cfg->n_persist >= c->Hkv)
+      return fail(CLO_ERR_INVALID, "n_persist must be in [0, n_kv_heads)");
+    if (cfg->persist_mask) return fail(CLO_ERR_INVALID, "persist_mask is only used with fixed tau");
+    c->W = cfg->warmup_steps;
+    c->P = cfg->n_persist;
+  } else {
+    int pmax = 0;
+    if (cfg->persist_mask) {
+      for (int l = 0; l < c->L; ++l) {
+        int n = 0;
+        for (int h = 0; h < c->Hkv; ++h) n += cfg->persist_mask[l * c->Hkv + h] ? 1 : 0;
+        pmax = std::max(pmax, n);
+      }
+    }
+    c->P = pmax;
+    c->warmup_done = true;
+  }
+  c->Nmax = cfg->max_tokens;
+  c->kmax = topk_for(c->Nmax, cfg->topk, cfg->topk_ratio);
+  c->U = (int64_t)c->L * c->B * c->Hkv;
+  c->stream = static_cast<cudaStream_t>(cfg->stream);
+  c->ntok.assign((size_t)c->L * c->B, 0);
+
+  int dev = 0;
+  CLO_CUDA(cudaGetDevice(&dev));
+  int can_map = 0;
+  CLO_CUDA(cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev));
+  if (!can_map) return fail(CLO_ERR_CUDA, "device cannot map host memory");
+
+  // pinned, device-mapped host pool: [U][Nmax][K|V]
+  const size_t rec = (size_t)4 * c->d;
+  const size_t pool_bytes = (size_t)c->U * (size_t)c->Nmax * rec;
+  void* hp = nullptr;
+  cudaError_t e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess)
+    return fail(CLO_ERR_OOM, "cudaHostAlloc(" + std::to_string(pool_bytes) + " B pinned pool): " + cudaGetErrorString(e));
+  c->pool_host = static_cast<uint16_t*>(hp);
+  void* pd = nullptr;
+  CLO_CUDA(cudaHostGetDevicePointer(&pd, hp, 0));
+  CLO_CUDA(cudaHostAlloc((void**)&c->ntok_pinned, sizeof(int64_t) * 2 * c->B, cudaHostAllocDefault));
+
+  DevState& s = c->ds;
+  s.L = c->L;
+  s.B = c->B;
+  s.Hq = c->Hq;
+  s.Hkv = c->Hkv;
+  s.d = c->d;
+  s.G = c->G;
+  s.P = c->P;
+  s.Nmax = c->Nmax;
+  s.kmax = c->kmax;
+  s.pool = static_cast<const uint16_t*>(pd);
+  s.wait_timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : 2000000000LL;
+  s.drop_flag_layer = cfg->debug_drop_flag_layer;
+  s.split_rows = kSplitRows;
+  s.nsplit = (int)((c->kmax + kSplitRows - 1) / kSplitRows);
+  const int64_t U = c->U;
+  const int LH = c->L * c->Hkv;
+  int64_t* ntok_d = nullptr;
+  int32_t* kcount_d = nullptr;
+  uint16_t* R_d = nullptr;
+  CLO_TRY(c->dalloc(&ntok_d, c->B));
+  CLO_TRY(c->dalloc(&kcount_d, c->B));
+  s.ntok = ntok_d;
+  s.kcount = kcount_d;
+  CLO_TRY(c->dalloc(&R_d, (size_t)LH * c->d * 128));
+  CLO_CUDA(cudaMemcpy(R_d, cfg->hash_R, sizeof(uint16_t) * (size_t)LH * c->d * 128, cudaMemcpyHostToDevice));
+  s.R = R_d;
+  CLO_TRY(c->dalloc(&s.codes, (size_t)U * c->Nmax));
+  CLO_TRY(c->dalloc(&s.qcodes, (size_t)c->L * c->B * c->Hq));
+  CLO_TRY(c->dalloc(&s.qcache, (size_t)U * c->G * c->d));
+  CLO_TRY(c->dalloc(&s.qvalid, (size_t)U));
+  CLO_TRY(c->dalloc(&s.tau, (size_t)LH));
+  CLO_TRY(c->dalloc(&s.persist, (size_t)LH));
+  CLO_TRY(c->dalloc(&s.persist_slot, (size_t)LH));
+  CLO_TRY(c->dalloc(&s.shat_sum, (size_t)LH));
+  CLO_TRY(c->dalloc(&s.shat, (size_t)LH));
+  CLO_TRY(c->dalloc(&s.decision, (size_t)U));
+  CLO_TRY(c->dalloc(&s.cosv, (size_t)U));
+  CLO_TRY(c->dalloc(&s.idx, (size_t)U * c->kmax));
+  CLO_TRY(c->dalloc(&s.slots, (size_t)U * c->kmax * 2 * c->d));
+  if (c->P > 0) {
+    CLO_TRY(c->dalloc(&s.resident, (size_t)c->L * c->B * c->P * c->Nmax * 2 * c->d));
+  } else {
+    s.resident = nullptr;
+  }
+  CLO_TRY(c->dalloc(&s.step_ctr, (size_t)C_NUM));
+  CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM));
+  CLO_TRY(c->dalloc(&s.err, 1));
+  CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));
+  CLO_TRY(c->dalloc(&s.ready, (size_t)U));
+  CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * c->G * (c->d + 2)));
+
+  std::vector<int32_t> pslot((size_t)LH, -1);
+  std::vector<uint8_t> pm((size_t)LH, 0);
+  if (!c->warmup_mode) {
+    CLO_CUDA(cudaMemcpy(s.tau, cfg->tau, sizeof(float) * LH, cudaMemcpyHostToDevice));
+    if (cfg->persist_mask) {
+      for (int l = 0; l < c->L; ++l) {
+        int p = 0;
+        for (int h = 0; h < c->Hkv; ++h)
+          if (cfg->persist_mask[l * c->Hkv + h]) {
+            pm[(size_t)l * c->Hkv + h] = 1;
+            pslot[(size_t)l * c->Hkv + h] = p++;
+          }
+      }
+    }
+    c->persist_host = pm;
+    c->persist_host_valid = true;
+  }
+  CLO_CUDA(cudaMemcpy(s.persist, pm.data(), LH, cudaMemcpyHostToDevice));
+  CLO_CUDA(cudaMemcpy(s.persist_slot, pslot.data(), sizeof(int32_t) * LH, cudaMemcpyHostToDevice));
+
+  CLO_TRY(c->dalloc(&c->kstage, (size_t)kStageTokens * c->Hkv * c->d));
+  CLO_TRY(c->dalloc(&c->vstage, (size_t)kStageTokens * c->Hkv * c->d));
+  for (auto& ev : c->ev) CLO_CUDA(cudaEventCreate(&ev));
+  c->have_events = true;
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_init(const clo_config* cfg, clo_ctx** out) {
+  if (!cfg || !out) return fail(CLO_ERR_INVALID, "null argument");
+  *out = nullptr;
+  clo_ctx* c = new (std::nothrow) clo_ctx();
+  if (!c) return fail(CLO_ERR_OOM, "context allocation");
+  clo_status st = init_impl(cfg, c);
+  if (st != CLO_OK) {
+    const std::string msg = g_last_error;
+    c->release();
+    delete c;
+    g_last_error = msg;
+    return st;
+  }
+  *out = c;
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_destroy(clo_ctx* ctx) {
+  if (!ctx) return CLO_OK;
+  ctx->release();
+  delete ctx;
+  return CLO_OK;
+}
+
+static clo_status read_device_error(clo_ctx* c) {
+  uint32_t err = 0;
+  CLO_CUDA(cudaMemcpy(&err, c->ds.err, sizeof(err), cudaMemcpyDeviceToHost));
+  if (err == 0) return CLO_OK;
+  CLO_CUDA(cudaMemset(c->ds.err, 0, sizeof(uint32_t)));
+  if (err & kErrFlagTimeout) return fail(CLO_ERR_TIMEOUT, "a ready-flag wait gave up (fetch never signalled)");
+  if (err & kErrMbarTimeout) return fail(CLO_ERR_TIMEOUT, "a bulk-copy barrier wait gave up");
+  return fail(CLO_ERR_DEVICE, "device-side bounds check failed (error word " + std::to_string(err) + ")");
+}
+
+CLO_API clo_status clo_sync(clo_ctx* c) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  CLO_CUDA(cudaStreamSynchronize(c->stream));
+  return read_device_error(c);
+}
+
+CLO_API clo_status clo_append_kv(clo_ctx* c, int32_t layer, int32_t seq, const void* k, const void* v,
+                                 int64_t n_tokens, int32_t src_is_device) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  if (layer < 0 || layer >= c->L || seq < 0 || seq >= c->B) return fail(CLO_ERR_INVALID, "layer/seq out of range");
+  if (n_tokens < 0 || (n_tokens > 0 && (!k || !v))) return fail(CLO_ERR_INVALID, "bad k/v/n_tokens");
+  int64_t& cur = c->ntok[(size_t)layer * c->B + seq];
+  if (cur + n_tokens > c->Nmax)
+    return fail(CLO_ERR_CAPACITY, "append of " + std::to_string(n_tokens) + " tokens exceeds max_tokens " +
+                                      std::to_string(c->Nmax) + " (current " + std::to_string(cur) + ")");
+  if (n_tokens == 0) return CLO_OK;
+  const size_t row = (size_t)c->Hkv * c->d;  // elements per token
+  for (int64_t t = 0; t < n_tokens; t += kStageTokens) {
+    const int64_t n = std::min<int64_t>(kStageTokens, n_tokens - t);
+    const uint16_t* ks = static_cast<const uint16_t*>(k) + (size_t)t * row;
+    const uint16_t* vs = static_cast<const uint16_t*>(v) + (size_t)t * row;
+    const uint16_t *kd = ks, *vd = vs;
+    if (!src_is_device) {
+      CLO_CUDA(cudaMemcpyAsync(c->kstage, ks, sizeof(uint16_t) * n * row, cudaMemcpyHostToDevice, c->stream));
+      CLO_CUDA(cudaMemcpyAsync(c->vstage, vs, sizeof(uint16_t) * n * row, cudaMemcpyHostToDevice, c->stream));
+      kd = c->kstage;
+      vd = c->vstage;
+    }
+    CLO_CUDA(launch_pool_write(c->ds, layer, seq, cur + t, n, kd, vd, c->stream));
+    CLO_CUDA(launch_hash_keys(c->ds, layer, seq, cur + t, n, kd, c->stream));
+    if (!src_is_device) CLO_CUDA(cudaStreamSynchronize(c->stream));  // staging is reused
+  }
+  CLO_CUDA(cudaStreamSynchronize(c->stream));
+  cur += n_tokens;
+  c->ntok_dirty = true;
+  return read_device_error(c);
+}
+
+static clo_status refresh_lengths(clo_ctx* c) {
+  int64_t nmax = 0;
+  for (int b = 0; b < c->B; ++b) {
+    const int64_t n0 = c->ntok[b];
+    for (int l = 1; l < c->L; ++l)
+      if (c->ntok[(size_t)l * c->B + b] != n0)
+        return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has layers of different lengths");
+    if (n0 < 1) return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has no K/V appended");
+    c->ntok_pinned[b] = n0;
+    nmax = std::max(nmax, n0);
+  }
+  int32_t* kc = reinterpret_cast<int32_t*>(c->ntok_pinned + c->B);
+  for (int b = 0; b < c->B; ++b) kc[b] = (int32_t)topk_for(c->ntok[b], c->cfg.topk, c->cfg.topk_ratio);
+  CLO_CUDA(cudaMemcpyAsync(const_cast<int64_t*>(c->ds.ntok), c->ntok_pinned, sizeof(int64_t) * c->B,
+                           cudaMemcpyHostToDevice, c->stream));
+  CLO_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(c->ds.kcount), kc, sizeof(int32_t) * c->B, cudaMemcpyHostToDevice,
+                           c->stream));
+  CLO_CUDA(cudaStreamSynchronize(c->stream));  // the pinned staging is reused
+  // cluster of CTAs per unit for the selection: chunks of about 16K tokens, <= 8 CTAs
+  int C = 1;
+  while (C < 8 && (nmax + C - 1) / C > kSelTargetChunk) C *= 2;
+  int64_t chunk = (nmax + C - 1) / C;
+  chunk = (chunk + kSelTile - 1) / kSelTile * kSelTile;
+  c->sel_cluster = C;
+  c->sel_chunk = chunk;
+  c->ntok_dirty = false;
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_t io_on_device) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  if (!q || !out) return fail(CLO_ERR_INVALID, "null q/out");
+  if (c->ntok_dirty) CLO_TRY(refresh_lengths(c));
+  const size_t nq = (size_t)c->L * c->B * c->Hq * c->d;
+  const uint16_t* qd = static_cast<const uint16_t*>(q);
+  float* od = out;
+  if (!io_on_device) {
+    if (!c->q_io) {
+      CLO_TRY(c->dalloc(&c->q_io, nq));
+      CLO_TRY(c->dalloc(&c->out_io, nq));
+    }
+    CLO_CUDA(cudaMemcpyAsync(c->q_io, q, sizeof(uint16_t) * nq, cudaMemcpyHostToDevice, c->stream));
+    qd = c->q_io;
+    od = c->out_io;
+  }
+  DevState& s = c->ds;
+  const bool warm = c->warmup_mode && c->step < c->W;
+  const bool timed = c->cfg.timing != 0;
+  ++c->epoch;
+  if (timed) CLO_CUDA(cudaEventRecord(c->ev[0], c->stream));
+  CLO_CUDA(cudaMemsetAsync(s.step_ctr, 0, sizeof(unsigned long long) * C_NUM, c->stream));
+  CLO_CUDA(launch_decide(s, qd, c->step, warm ? 1 : 0, c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(c->ev[1], c->stream));
+  CLO_CUDA(launch_select(s, c->sel_cluster, c->sel_chunk, c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(c->ev[2], c->stream));
+  CLO_CUDA(launch_gather(s, c->epoch, c->stream));
+  CLO_CUDA(launch_attend(s, qd, od, c->epoch, c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(c->ev[3], c->stream));
+  if (warm && c->step == c->W - 1) {
+    CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
+    CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
+    c->warmup_done = true;
+    c->persist_host_valid = false;
+  }
+  c->step_timed = timed;
+  ++c->step;
+  if (!io_on_device) {
+    CLO_CUDA(cudaMemcpyAsync(out, c->out_io, sizeof(float) * nq, cudaMemcpyDeviceToHost, c->stream));
+    return clo_sync(c);
+  }
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
+  if (!c || !out) return fail(CLO_ERR_INVALID, "null argument");
+  CLO_CUDA(cudaStreamSynchronize(c->stream));
+  unsigned long long last[C_NUM], tot[C_NUM];
+  CLO_CUDA(cudaMemcpy(last, c->ds.step_ctr, sizeof(last), cudaMemcpyDeviceToHost));
+  CLO_CUDA(cudaMemcpy(tot, c->ds.total_ctr, sizeof(tot), cudaMemcpyDeviceToHost));
+  std::memset(out, 0, sizeof(*out));
+  out->steps = c->step;
+  out->units_hit = (int64_t)tot[C_HIT];
+  out->units_miss = (int64_t)tot[C_MISS];
+  out->units_persist = (int64_t)tot[C_PERSIST];
+  out->host_bytes = (int64_t)tot[C_HOST_BYTES];
+  out->hbm_bytes_alg = (int64_t)tot[C_HBM_BYTES];
+  out->timeouts = (int64_t)tot[C_TIMEOUTS];
+  out->last_hit = (int64_t)last[C_HIT];
+  out->last_miss = (int64_t)last[C_MISS];
+  out->last_persist = (int64_t)last[C_PERSIST];
+  out->last_host_bytes = (int64_t)last[C_HOST_BYTES];
+  out->last_hbm_bytes_alg = (int64_t)last[C_HBM_BYTES];
+  out->warmup_done = c->warmup_done ? 1 : 0;
+  if (c->step_timed && c->step > 0) {
+    cudaEventElapsedTime(&out->last_ms_decide, c->ev[0], c->ev[1]);
+    cudaEventElapsedTime(&out->last_ms_select, c->ev[1], c->ev[2]);
+    cudaEventElapsedTime(&out->last_ms_fetch_attend, c->ev[2], c->ev[3]);
+    cudaEventElapsedTime(&out->last_ms_total, c->ev[0], c->ev[3]);
+  }
+  return read_device_error(c);
+}
+
+CLO_API clo_status clo_debug_get(clo_ctx* c, int32_t what, int32_t layer, int32_t seq, int32_t kvh, void* dst,
+                                 int64_t dst_bytes) {
+  if (!c || !dst) return fail(CLO_ERR_INVALID, "null argument");
+  const bool per_unit = what == CLO_DBG_KEY_CODES || what == CLO_DBG_QUERY_CODES || what == CLO_DBG_IDX ||
+                        what == CLO_DBG_SLOT_ROWS;
+  if (per_unit && (layer < 0 || layer >= c->L || seq < 0 || seq >= c->B || kvh < 0 || kvh >= c->Hkv))
+    return fail(CLO_ERR_INVALID, "unit out of range");
+  CLO_CUDA(cudaStreamSynchronize(c->stream));
+  const DevState& s = c->ds;
+  const int64_t u = ((int64_t)layer * c->B + seq) * c->Hkv + kvh;
+  const int64_t N = per_unit ? c->ntok[(size_t)layer * c->B + seq] : 0;
+  const int64_t k = per_unit ? topk_for(N, c->cfg.topk, c->cfg.topk_ratio) : 0;
+  const void* src = nullptr;
+  int64_t bytes = 0;
+  switch (what) {
+    case CLO_DBG_KEY_CODES:
+      src = s.codes + u * c->Nmax;
+      bytes = N * 16;
+      break;
+    case CLO_DBG_QUERY_CODES:
+      src = s.qcodes + ((int64_t)layer * c->B + seq) * c->Hq + (int64_t)kvh * c->G;
+      bytes = (int64_t)c->G * 16;
+      break;
+    case CLO_DBG_IDX:
+      src = s.idx + u * c->kmax;
+      bytes = k * 4;
+      break;
+    case CLO_DBG_DECISION:
+      src = s.decision;
+      bytes = c->U;
+      break;
+    case CLO_DBG_SLOT_ROWS:
+      src = s.slots + u * c->kmax * 2 * c->d;
+      bytes = k * 4 * c->d;
+      break;
+    case CLO_DBG_TAU:
+      src = s.tau;
+      bytes = (int64_t)c->L * c->Hkv * 4;
+      break;
+    case CLO_DBG_PERSIST:
+      src = s.persist;
+      bytes = (int64_t)c->L * c->Hkv;
+      break;
+    case CLO_DBG_SHAT:
+      src = s.shat;
+      bytes = (int64_t)c->L * c->Hkv * 8;
+      break;
+    case CLO_DBG_COS:
+      src = s.cosv;
+      bytes = c->U * 4;
+      break;
+    default:
+      return fail(CLO_ERR_INVALID, "unknown debug item " + std::to_string(what));
+  }
+  if (dst_bytes < bytes)
+    return fail(CLO_ERR_INVALID, "dst too small: need " + std::to_string(bytes) + " bytes");
+  CLO_CUDA(cudaMemcpy(dst, src, (size_t)bytes, cudaMemcpyDeviceToHost));
+  return read_device_error(c);
+}
+
+CLO_API clo_status clo_set(clo_ctx* c, int32_t key, int64_t value) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  switch (key) {
+    case CLO_SET_DROP_FLAG_LAYER:
+      c->ds.drop_flag_layer = (int)value;
+      c->cfg.debug_drop_flag_layer = (int32_t)value;
+      return CLO_OK;
+    case CLO_SET_WAIT_TIMEOUT_NS:
+      if (value <= 0) return fail(CLO_ERR_INVALID, "timeout must be > 0");
+      c->ds.wait_timeout_ns = value;
+      c->cfg.wait_timeout_ns = value;
+      return CLO_OK;
+    default:
+      return fail(CLO_ERR_INVALID, "unknown setting " + std::to_string(key));
+  }
+}
+
+}  // extern "C"

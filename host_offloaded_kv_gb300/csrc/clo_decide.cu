@@ -1,0 +1,197 @@
+// Head-wise reuse decision and query hashing (one CTA per unit).
+//
+// Reuse test: adjacent-step query cosine similarity is high (> 0.8) on most
+// heads, which CLO turns into a cache-reuse condition ("CLO (2511.14510) - L3
+// Per-Paper Synthesis", section 2.1 item 2; CLO abstract, feature (1):
+// coarse-grained head-wise approximate on-GPU caching).  A unit reuses its
+// previous selection iff cos(q_group, q_cached) >= tau[l][h], q_cached being the
+// query of the unit's last refresh.  Persistent heads always reselect (CLO
+// abstract, feature (2)).  Thresholds and persistent heads come from profiling
+// (section 3.3 attack 6: s_hat_i, D_i, N_persist): warm-up steps reselect every
+// unit and accumulate cos(q_t, q_{t-1}).
+#include "clo_hash.cuh"
+#include "clo_internal.cuh"
+
+namespace clo {
+
+namespace {
+
+constexpr int kDecideThreads = 128;
+
+struct StridedF32 {
+  const float* p;
+  int stride;
+  __device__ float operator()(int i) const { return p[i * stride]; }
+};
+struct StridedBF16 {
+  const uint16_t* p;
+  int stride;
+  __device__ float operator()(int i) const { return bf16_bits_to_f32(p[i * stride]); }
+};
+
+__global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uint16_t* __restrict__ q, int64_t step,
+                                                            int warmup_active) {
+  __shared__ float qs[kMaxG * kMaxD];
+  __shared__ float red[3][kDecideThreads / 32];
+  __shared__ int s_dec;
+  __shared__ uint32_t words[kMaxG][4];
+
+  const int64_t u = blockIdx.x;
+  const int h = (int)(u % s.Hkv);
+  const int b = (int)((u / s.Hkv) % s.B);
+  const int l = (int)(u / ((int64_t)s.Hkv * s.B));
+  const int G = s.G, d = s.d, GD = s.G * s.d;
+  const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * d;
+  uint16_t* qc = s.qcache + u * GD;
+
+  float dot = 0.f, nq = 0.f, nc = 0.f;
+  for (int e = threadIdx.x; e < GD; e += kDecideThreads) {
+    const float x = bf16_bits_to_f32(qg[e]);
+    const float c = bf16_bits_to_f32(qc[e]);
+    qs[e] = x;
+    dot = fmaf(x, c, dot);
+    nq = fmaf(x, x, nq);
+    nc = fmaf(c, c, nc);
+  }
+  dot = warp_sum(dot);
+  nq = warp_sum(nq);
+  nc = warp_sum(nc);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[0][warp] = dot;
+    red[1][warp] = nq;
+    red[2][warp] = nc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float D = 0.f, Q = 0.f, C = 0.f;
+    for (int w = 0; w < kDecideThreads / 32; ++w) {
+      D += red[0][w];
+      Q += red[1][w];
+      C += red[2][w];
+    }
+    const bool valid = s.qvalid[u] != 0;
+    float cosv = (Q > 0.f && C > 0.f) ? D / (sqrtf(Q) * sqrtf(C)) : 0.f;
+    const int lh = l * s.Hkv + h;
+    int dec;
+    if (warmup_active) {
+      dec = CLO_DEC_MISS;
+      if (step >= 1 && valid) atomicAdd(&s.shat_sum[lh], (double)cosv);
+    } else if (s.persist[lh]) {
+      dec = CLO_DEC_PERSIST;
+    } else if (!valid) {
+      dec = CLO_DEC_MISS;
+    } else {
+      dec = (cosv >= s.tau[lh]) ? CLO_DEC_HIT : CLO_DEC_MISS;
+    }
+    s.decision[u] = (uint8_t)dec;
+    s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
+    s_dec = dec;
+
+    // counters: decisions, host bytes, algorithmic HBM bytes of this unit's step
+    const int64_t N = s.ntok[b];
+    const int64_t k = s.kcount[b];
+    const int64_t rec = 4LL * d;
+    unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
+    int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
+    if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
+    if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
+    if (dec == CLO_DEC_PERSIST) hbm += k * 4;
+    const int slot = dec == CLO_DEC_HIT ? C_HIT : (dec == CLO_DEC_MISS ? C_MISS : C_PERSIST);
+    atomicAdd(&s.step_ctr[slot], 1ull);
+    atomicAdd(&s.total_ctr[slot], 1ull);
+    if (host) {
+      atomicAdd(&s.step_ctr[C_HOST_BYTES], host);
+      atomicAdd(&s.total_ctr[C_HOST_BYTES], host);
+    }
+    atomicAdd(&s.step_ctr[C_HBM_BYTES], (unsigned long long)hbm);
+    atomicAdd(&s.total_ctr[C_HBM_BYTES], (unsigned long long)hbm);
+  }
+  __syncthreads();
+  const int dec = s_dec;
+  if (dec == CLO_DEC_MISS) {
+    for (int e = threadIdx.x; e < GD; e += kDecideThreads) qc[e] = qg[e];
+    if (threadIdx.x == 0) s.qvalid[u] = 1;
+  }
+  if (dec == CLO_DEC_HIT) return;
+
+  // query codes of the G heads: thread j computes bit j of every head
+  const int j = threadIdx.x;  // 128 threads = 128 bits
+  const uint16_t* Rg = s.R + ((int64_t)l * s.Hkv + h) * d * 128;
+  float acc[kMaxG], aab[kMaxG];
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g) acc[g] = aab[g] = 0.f;
+  for (int i = 0; i < d; ++i) {
+    const float r = bf16_bits_to_f32(Rg[i * 128 + j]);
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g) {
+      if (g < G) {
+        const float x = qs[g * d + i];
+        acc[g] = fmaf(x, r, acc[g]);
+        aab[g] = fmaf(fabsf(x), fabsf(r), aab[g]);
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g) {
+    if (g < G) {
+      bool bit;
+      if (sign_certified_f32(acc[g], aab[g], d))
+        bit = acc[g] > 0.f;
+      else
+        bit = hash_bit_slow(StridedF32{qs + g * d, 1}, StridedBF16{Rg + j, 128}, d);
+      const uint32_t w = __ballot_sync(0xffffffffu, bit);
+      if (lane == 0) words[g][warp] = w;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
+    s.qcodes[((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G + g] =
+        make_uint4(words[g][0], words[g][1], words[g][2], words[g][3]);
+  }
+}
+
+// End of warm-up: s_hat = mean adjacent-step cosine, tau = s_hat - offset, and the
+// n_persist lowest-s_hat heads of each layer (ties: lower head index) persistent.
+__global__ void k_finish_warmup(DevState s, int W, float tau_offset, int n_persist) {
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  if (l >= s.L) return;
+  const double npairs = (double)s.B * (double)(W - 1);
+  for (int h = 0; h < s.Hkv; ++h) {
+    const int lh = l * s.Hkv + h;
+    const double sh = s.shat_sum[lh] / npairs;
+    s.shat[lh] = sh;
+    s.tau[lh] = (float)(sh - (double)tau_offset);
+    s.persist[lh] = 0;
+    s.persist_slot[lh] = -1;
+  }
+  for (int p = 0; p < n_persist; ++p) {
+    int best = -1;
+    for (int h = 0; h < s.Hkv; ++h) {
+      const int lh = l * s.Hkv + h;
+      if (s.persist[lh]) continue;
+      if (best < 0 || s.shat[lh] < s.shat[l * s.Hkv + best]) best = h;
+    }
+    if (best >= 0) s.persist[l * s.Hkv + best] = 1;
+  }
+  int p = 0;
+  for (int h = 0; h < s.Hkv; ++h)
+    if (s.persist[l * s.Hkv + h]) s.persist_slot[l * s.Hkv + h] = p++;
+}
+
+}  // namespace
+
+cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active,
+                          cudaStream_t st) {
+  const int64_t U = (int64_t)s.L * s.B * s.Hkv;
+  k_decide<<<(unsigned)U, kDecideThreads, 0, st>>>(s, q, step, warmup_active);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st) {
+  k_finish_warmup<<<(s.L + 63) / 64, 64, 0, st>>>(s, W, tau_offset, n_persist);
+  return cudaGetLastError();
+}
+
+}  // namespace clo

@@ -1,0 +1,190 @@
+// Internal declarations shared by the CLO kernels and the host runtime.
+//
+// Data layout (all per context; unit u = (l * B + b) * Hkv + h):
+//   host pool (pinned, device-mapped)  bf16 [U][Nmax][K(d) | V(d)]  record = 4*d bytes
+//   codes      (HBM)                   uint4 [U][Nmax]               128-bit key codes
+//   qcodes     (HBM)                   uint4 [L][B][Hq]              query codes of the step
+//   qcache     (HBM)                   bf16 [U][G*d]                 query at the last refresh
+//   idx        (HBM)                   int32 [U][kmax]               selection, ascending
+//   slots      (HBM)                   bf16 [U][kmax][K | V]         on-GPU cache of fetched rows
+//   resident   (HBM)                   bf16 [L][B][P][Nmax][K | V]   persistent heads' full K/V
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "clo.h"
+
+namespace clo {
+
+constexpr int kMaxG = 8;
+constexpr int kMaxD = 128;
+constexpr int64_t kMaxTokens = 524288;
+
+// device error word bits
+constexpr uint32_t kErrFlagTimeout = 1u;   // a ready-flag wait gave up
+constexpr uint32_t kErrMbarTimeout = 2u;   // a bulk-copy barrier wait gave up
+constexpr uint32_t kErrBounds = 4u;        // an internal bounds check failed
+
+// step counters (uint64 slots)
+enum Counter : int {
+  C_HIT = 0,
+  C_MISS = 1,
+  C_PERSIST = 2,
+  C_HOST_BYTES = 3,
+  C_HBM_BYTES = 4,
+  C_TIMEOUTS = 5,
+  C_NUM = 8
+};
+
+struct DevState {
+  int L, B, Hq, Hkv, d, G;
+  int P;                        // resident heads per layer allocated (0 = none)
+  int64_t Nmax, kmax;
+  const int64_t* ntok;          // [B]
+  const int32_t* kcount;        // [B]
+  const uint16_t* R;            // [L][Hkv][d][128]
+  uint4* codes;                 // [U][Nmax]
+  uint4* qcodes;                // [L][B][Hq]
+  uint16_t* qcache;             // [U][G*d]
+  uint8_t* qvalid;              // [U]
+  float* tau;                   // [L*Hkv]
+  uint8_t* persist;             // [L*Hkv]
+  int32_t* persist_slot;        // [L*Hkv] resident index or -1
+  double* shat_sum;             // [L*Hkv]
+  double* shat;                 // [L*Hkv]
+  uint8_t* decision;            // [U]
+  float* cosv;                  // [U]
+  int32_t* idx;                 // [U][kmax]
+  uint16_t* slots;              // [U][kmax][2d]
+  uint16_t* resident;           // [L][B][P][Nmax][2d]
+  const uint16_t* pool;         // device view of the host pool [U][Nmax][2d]
+  unsigned long long* step_ctr; // [C_NUM] this step
+  unsigned long long* total_ctr;// [C_NUM] since init
+  uint32_t* err;                // error word
+  uint32_t* unit_done;          // [U] split counters of the attention combine
+  float* part;                  // attention partials [U][nsplit][G][d + 2]
+  int nsplit;                   // attention splits per unit
+  int split_rows;               // rows per split
+  uint32_t* ready;              // [U] fetch-ready epochs
+  int64_t wait_timeout_ns;
+  int drop_flag_layer;
+};
+
+__host__ __device__ inline int64_t unit_of(const DevState& s, int l, int b, int h) {
+  return ((int64_t)l * s.B + b) * s.Hkv + h;
+}
+
+// ---------------------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; on timeout sets kErrMbarTimeout and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrMbarTimeout);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------- launchers
+// (each returns the launch's cudaError_t)
+cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
+                             cudaStream_t st);
+cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st);
+cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st);
+cudaError_t launch_select(const DevState& s, int cluster, int64_t chunk, cudaStream_t st);
+cudaError_t launch_gather(const DevState& s, uint32_t epoch, cudaStream_t st);
+cudaError_t launch_attend(const DevState& s, const uint16_t* q, float* out, uint32_t epoch, cudaStream_t st);
+cudaError_t launch_resident_fill(const DevState& s, int64_t t0, int64_t t1, cudaStream_t st);
+cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
+                              const uint16_t* vdev, cudaStream_t st);
+
+size_t select_smem_bytes(int G, int64_t chunk);
+
+}  // namespace clo

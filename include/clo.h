@@ -1,0 +1,198 @@
+/*
+ * clo.h -- C ABI of the CLO decode-step library for GB300 (sm_103a).
+ *
+ * CLO is a CPU-light KV-cache offloading system: the full K/V cache of every
+ * sequence lives in pinned host memory, and each decode step attends only to the
+ * top-k (10 %) tokens of each KV head, chosen by a hash-code scorer.  A head whose
+ * query barely moved since its last refresh reuses its previous on-GPU selection;
+ * a few "persistent" heads stay fully resident in HBM; everything else is fetched
+ * from host memory by GPU loads, with no CPU thread on the data path.
+ *
+ * Sources (page title, section):
+ *   [ABS] CLO abstract (arXiv 2511.14510v1, paper-check page): KV in CPU memory
+ *         with top-k attention; features (1) head-wise approximate on-GPU cache,
+ *         (2) prefetching combined with on-GPU persistent caching, (3) zero-copy
+ *         transfer engine and GPU-centric synchronisation.
+ *   [SYN] "CLO (2511.14510) - L3 Per-Paper Synthesis": section 2.1 (query cosine
+ *         similarity > 0.8 between adjacent steps as the reuse condition; UVA
+ *         polling), 2.2 (top-k = 10 %), 3.2 (HATA top-k scorer), 3.3 attack 6
+ *         (s_hat_i, D_i, N_persist from profiling), 5.6 (prefetch one layer ahead),
+ *         5.7 (KV produced at prefill and offloaded once).
+ *
+ * Conventions
+ *   - Every call returns a clo_status; nothing aborts, throws or traps.  The text
+ *     of the last error of the calling thread is returned by clo_last_error().
+ *   - Element type is bf16 (uint16 bit patterns) for K, V, queries and the hash
+ *     projection; attention outputs are fp32.
+ *   - A "unit" is one (layer, sequence, kv head).  G = n_q_heads / n_kv_heads
+ *     query heads share a unit (GQA).
+ *   - Device pointers passed in stay owned by the caller; the library owns all
+ *     memory it allocates (pinned host pool, HBM buffers) and frees it in
+ *     clo_destroy().
+ *   - Device-side failures (a ready-flag wait that ran out of time, an internal
+ *     bounds check) are latched in a device error word and reported by the next
+ *     call that synchronises with the stream: clo_sync(), clo_stats(), a
+ *     host-buffer clo_decode_step(), or clo_debug_get().
+ */
+#ifndef CLO_H_
+#define CLO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CLO_API __attribute__((visibility("default")))
+#else
+#define CLO_API
+#endif
+
+typedef struct clo_ctx clo_ctx; /* opaque */
+
+typedef enum {
+  CLO_OK = 0,
+  CLO_ERR_INVALID = 1,  /* bad argument or configuration */
+  CLO_ERR_OOM = 2,      /* host (pinned) or device allocation failed */
+  CLO_ERR_CUDA = 3,     /* a CUDA runtime call failed */
+  CLO_ERR_TIMEOUT = 4,  /* a device-side ready-flag wait gave up (bounded wait) */
+  CLO_ERR_STATE = 5,    /* call not valid in the context's current state */
+  CLO_ERR_CAPACITY = 6, /* append beyond max_tokens */
+  CLO_ERR_DEVICE = 7    /* a device-side bounds check failed */
+} clo_status;
+
+/* Reuse decision of a unit in one step (as read back by clo_debug_get). */
+enum { CLO_DEC_HIT = 0, CLO_DEC_MISS = 1, CLO_DEC_PERSIST = 2 };
+
+typedef struct clo_config {
+  int32_t n_layers;   /* L >= 1 */
+  int32_t batch;      /* B >= 1 sequences */
+  int32_t n_q_heads;  /* Hq, multiple of n_kv_heads, G = Hq/Hkv <= 8 */
+  int32_t n_kv_heads; /* Hkv >= 1 */
+  int32_t head_dim;   /* d: 64 or 128 */
+  int64_t max_tokens; /* capacity per sequence (sizes the pinned host pool); <= 524288 */
+  /* top-k budget: topk > 0 -> k = min(topk, N); else k = ceil(topk_ratio * N),
+   * evaluated as one IEEE double product, clamped to [1, N]  ([SYN] 2.2: 10 %) */
+  int64_t topk;
+  double topk_ratio;
+  /* hash projection R: host bf16 [L][Hkv][d][128] (row i, column j at i*128+j);
+   * required; copied.  Bit j of the code of x is 1 iff the exact real value of
+   * sum_i x_i R_ij is > 0 ([SYN] 3.2 names HATA as the top-k scorer). */
+  const uint16_t* hash_R;
+  /* reuse thresholds tau: host fp32 [L][Hkv], copied; NULL -> warm-up profiling:
+   * the first warmup_steps steps reselect every unit, s_hat[l][h] = mean over the
+   * batch and adjacent step pairs of cos(q_t, q_{t-1}), tau = s_hat - tau_offset,
+   * and the n_persist heads with the lowest s_hat per layer become persistent
+   * ([SYN] 3.3 attack 6; [SYN] 2.1 item 2). */
+  const float* tau;
+  /* persistent heads when tau is given: host uint8 [L][Hkv] (nonzero = resident),
+   * or NULL for none ([ABS] feature (2)). */
+  const uint8_t* persist_mask;
+  int32_t warmup_steps; /* >= 2 when tau == NULL (default 16) */
+  float tau_offset;     /* default 0.05 */
+  int32_t n_persist;    /* persistent heads per layer after warm-up, < Hkv */
+  int64_t wait_timeout_ns; /* bound of every device-side ready-flag wait; <= 0 -> 2 s */
+  int32_t timing;          /* nonzero: record per-phase CUDA-event times (clo_stats) */
+  int32_t debug_drop_flag_layer; /* fault injection: >= 0 -> the fetch of this layer
+                                    never signals its ready flags; -1 = off */
+  void* stream;            /* cudaStream_t to run on; NULL = the legacy default stream */
+} clo_config;
+
+typedef struct clo_stats_t {
+  int64_t steps;             /* decode steps completed */
+  int64_t units_hit;         /* cumulative unit decisions */
+  int64_t units_miss;
+  int64_t units_persist;
+  int64_t host_bytes;        /* bytes fetched from the host pool (K and V rows) */
+  int64_t hbm_bytes_alg;     /* algorithmic HBM bytes of the decode steps */
+  int64_t timeouts;          /* ready-flag waits that gave up */
+  int64_t last_hit, last_miss, last_persist, last_host_bytes, last_hbm_bytes_alg;
+  float last_ms_decide, last_ms_select, last_ms_fetch_attend, last_ms_total; /* timing != 0 */
+  int32_t warmup_done;       /* 1 once thresholds and persistent heads are fixed */
+} clo_stats_t;
+
+/* Fill *cfg with defaults (shapes zero; topk_ratio 0.1; warmup_steps 16;
+ * tau_offset 0.05; wait 2 s; debug_drop_flag_layer -1). */
+CLO_API void clo_config_default(clo_config* cfg);
+
+/* Create a context: allocates the pinned, device-mapped host K/V pool
+ * (L*B*Hkv*max_tokens records of K||V, 4*d bytes each, [SYN] 3.4 attack 7 sizes the
+ * pool of a 512K Qwen2.5-14B context at 93.75 GB) and the HBM state (hash codes,
+ * selections, cache slots, resident copies).  *out receives the context.
+ * Errors: CLO_ERR_INVALID (shapes), CLO_ERR_OOM, CLO_ERR_CUDA. */
+CLO_API clo_status clo_init(const clo_config* cfg, clo_ctx** out);
+
+/* Release everything the context owns.  NULL is accepted. */
+CLO_API clo_status clo_destroy(clo_ctx* ctx);
+
+/* Offload prefill K/V once ([SYN] 5.7: KV is produced at prefill and offloaded):
+ * appends n_tokens tokens of (layer, seq) at its current length.
+ * k, v: bf16 [n_tokens][Hkv][d], host (src_is_device = 0) or device (1) memory,
+ * copied; the caller keeps ownership and may reuse them on return.  Computes the
+ * keys' 128-bit hash codes on the GPU (kept in HBM).  Synchronous.
+ * Errors: CLO_ERR_INVALID, CLO_ERR_CAPACITY (length would exceed max_tokens),
+ * CLO_ERR_CUDA. */
+CLO_API clo_status clo_append_kv(clo_ctx* ctx, int32_t layer, int32_t seq, const void* k, const void* v,
+                                 int64_t n_tokens, int32_t src_is_device);
+
+/* One decode step over all layers ([ABS]; [SYN] 2.1, 2.2):
+ * q: bf16 [L][B][Hq][d]; out: fp32 [L][B][Hq][d].
+ * io_on_device = 1: q and out are device pointers; the call only enqueues work on
+ *   the context's stream and returns (no host synchronisation between layers or
+ *   at the end); device errors surface at the next synchronising call.
+ * io_on_device = 0: q and out are host pointers; the call copies q in, runs the
+ *   step, copies out back and waits for it, returning device errors directly.
+ * Every layer of every sequence must hold the same number of tokens (>= 1).
+ * Errors: CLO_ERR_INVALID, CLO_ERR_STATE (no K/V, or ragged layers),
+ * CLO_ERR_CUDA, CLO_ERR_TIMEOUT / CLO_ERR_DEVICE (host-buffer mode only). */
+CLO_API clo_status clo_decode_step(clo_ctx* ctx, const void* q, float* out, int32_t io_on_device);
+
+/* Wait for all work of the context and report a latched device error, if any
+ * (CLO_ERR_TIMEOUT or CLO_ERR_DEVICE); the latch is cleared once reported. */
+CLO_API clo_status clo_sync(clo_ctx* ctx);
+
+/* Counters since clo_init (synchronises; also reports a latched device error
+ * after filling *out). */
+CLO_API clo_status clo_stats(clo_ctx* ctx, clo_stats_t* out);
+
+/* Thread-local text of the last failed call ("" if none). */
+CLO_API const char* clo_last_error(void);
+
+/* Debug read-back of internal state (synchronises).  what selects the item;
+ * dst is a host buffer of dst_bytes bytes; layer/seq/kvh select the unit where
+ * the item is per unit.
+ *   CLO_DBG_KEY_CODES   uint64 [N][2] hash codes of the unit's keys
+ *   CLO_DBG_QUERY_CODES uint64 [G][2] query codes of the unit's last reselection
+ *   CLO_DBG_IDX         int32 [k]     current selection (ascending token index)
+ *   CLO_DBG_DECISION    uint8 [L][B][Hkv] decisions of the last step (unit ignored)
+ *   CLO_DBG_SLOT_ROWS   bf16 [k][2][d] the unit's on-GPU cache slot (K row, V row)
+ *   CLO_DBG_TAU         fp32 [L][Hkv] thresholds (after warm-up)
+ *   CLO_DBG_PERSIST     uint8 [L][Hkv] persistent mask
+ *   CLO_DBG_SHAT        fp64 [L][Hkv] warm-up mean similarity
+ *   CLO_DBG_COS         fp32 [L][B][Hkv] cosines of the last step (NaN if none)
+ * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
+enum {
+  CLO_DBG_KEY_CODES = 1,
+  CLO_DBG_QUERY_CODES = 2,
+  CLO_DBG_IDX = 3,
+  CLO_DBG_DECISION = 4,
+  CLO_DBG_SLOT_ROWS = 5,
+  CLO_DBG_TAU = 6,
+  CLO_DBG_PERSIST = 7,
+  CLO_DBG_SHAT = 8,
+  CLO_DBG_COS = 9
+};
+CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int32_t seq, int32_t kvh, void* dst,
+                                 int64_t dst_bytes);
+
+/* Change a debug setting after init (fault injection on the host side):
+ * key CLO_SET_DROP_FLAG_LAYER (value: layer or -1), CLO_SET_WAIT_TIMEOUT_NS. */
+enum { CLO_SET_DROP_FLAG_LAYER = 1, CLO_SET_WAIT_TIMEOUT_NS = 2 };
+CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CLO_H_ */

@@ -1,0 +1,77 @@
+"""CUDA library vs CPU oracle, element by element, on seeded inputs (needs a GPU).
+
+Bit-exact: key and query hash codes, top-k index sets, reuse decisions (except
+|cos - tau| < 1e-4), gathered rows, host byte counts.  Attention outputs: max abs
+error 2e-3 and relative L2 error 1e-3."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from clo_harness import LockStep, Spec  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(spec, steps, io_on_device=True):
+    ls = LockStep(spec)
+    try:
+        ls.check_key_codes()
+        for _ in range(steps):
+            ls.step(io_on_device=io_on_device)
+        return ls.log
+    finally:
+        ls.close()
+
+
+def test_tiny_workload_full_parity():
+    # 1 layer, batch 1, 8/2 heads, d 64, 4096 tokens, k 410, tau 0.8, 16 steps, seed 0
+    log = _run(Spec(L=1, B=1, Hq=8, Hkv=2, d=64, ntok=[4096], seed=0, topk=410, tau=0.8), 16)
+    assert sum(r["hit"] for r in log) > 0 and sum(r["miss"] for r in log) > 0
+
+
+def test_warmup_profiling_and_persistent_heads():
+    # warm-up thresholds, 1 persistent head per layer; G = 2, d = 128, several tiles
+    spec = Spec(L=2, B=2, Hq=8, Hkv=4, d=128, ntok=[6000, 6000], seed=5, tau=None, warmup_steps=4, n_persist=1)
+    log = _run(spec, 9)
+    assert all(r["persist"] == 4 for r in log[4:])
+    assert sum(r["hit"] for r in log[4:]) > 0
+
+
+def test_ragged_sequences_and_cluster_selection():
+    # three sequences of different lengths; the longest spans a 4-CTA cluster; G = 5
+    spec = Spec(L=1, B=3, Hq=10, Hkv=2, d=128, ntok=[40000, 17000, 3001], seed=7, tau=0.8, rho=(0.7, 0.98))
+    _run(spec, 4)
+
+
+def test_host_buffer_io_matches_device_io():
+    spec = Spec(L=1, B=2, Hq=4, Hkv=2, d=64, ntok=[3000, 2500], seed=9, tau=0.85)
+    _run(spec, 5, io_on_device=False)
+
+
+def test_topk_equals_context_is_dense_attention():
+    # k = N: every token selected; attention is plain softmax attention
+    spec = Spec(L=1, B=1, Hq=4, Hkv=1, d=64, ntok=[700], seed=11, topk=700, tau=2.0)
+    _run(spec, 2)
+
+
+def test_single_token_context():
+    spec = Spec(L=2, B=2, Hq=2, Hkv=1, d=64, ntok=[1, 1], seed=12, tau=0.5)
+    _run(spec, 3)
+
+
+def test_all_scores_tied_selects_lowest_indices():
+    # all-zero keys: every key code is 0 and every score ties -> selection {0..k-1}
+    L, B, Hkv, d, N = 1, 1, 2, 64, 5000
+    K = np.zeros((N, Hkv, d), dtype=np.uint16)
+    V = np.zeros((N, Hkv, d), dtype=np.uint16)
+    V[:, :, :] = np.arange(N, dtype=np.uint16)[:, None, None] & 0x3fff   # distinct finite values
+    spec = Spec(L=L, B=B, Hq=4, Hkv=Hkv, d=d, ntok=[N], seed=13, tau=2.0, kv_override={(0, 0): (K, V)})
+    ls = LockStep(spec)
+    try:
+        ls.check_key_codes()
+        ls.step()
+        k = ls.lib.k_of(0)
+        assert ls.lib.idx(0, 0, 0).tolist() == list(range(k))
+    finally:
+        ls.close()
