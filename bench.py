@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the CLO hot path (decoded tokens/s).
+
+Default workload: Llama3-8B-shaped attention stack, 32 layers, 32/8 heads,
+head_dim 128, batch 8, 32K-token context per sequence in pinned host memory,
+top-k 10 %, 4 persistent heads per layer, thresholds from 16 profiling steps.
+
+One step = one clo_decode_step over all layers (reuse test, query hashing,
+scoring + top-k, zero-copy fetch of missed rows, sparse attention), one decoded
+token per sequence.  The method's 16 profiling steps run before the W warm-up
+steps and are not timed (CLO profiles offline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama32k]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decoded tokens/s through offloaded top-k attention"
+UNIT = "tokens/s"
+
+
+def _env_int(name, default):
+    v = os.environ.get(name)
+    return int(v) if v not in (None, "") else default
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="llama32k")
+    p.add_argument("--layers", type=int, default=0, help="override the layer count (profiling runs only)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-steps", type=int, default=2, help="oracle steps timed for the CPU baseline")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def mem_available_bytes():
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch recorded by an ncu capture under profiles/, if the kernel's
+    source has not changed since (the summary stores the source digest)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    want, traffic = None, None
+    for line in txt.splitlines():
+        if line.startswith("source_sha256:"):
+            want = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            val = line.split(":", 1)[1].strip()
+            traffic = None if val in ("", "null") else float(val)
+    src = os.path.join(ROOT, "host_offloaded_kv_gb300", "csrc", "clo_attend.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if want != digest:
+        return None
+    return traffic
+
+
+# ----------------------------------------------------------------------------- workload
+def workload_from_args(args):
+    from host_offloaded_kv_gb300.synth import get_workload
+
+    w = get_workload(args.workload)
+    if args.layers:
+        w = w.scaled(n_layers=args.layers)
+    return w
+
+
+def topk_of(w):
+    if w.topk > 0:
+        return min(w.topk, w.n_tokens)
+    return max(1, min(w.n_tokens, int(math.ceil(w.topk_ratio * w.n_tokens))))
+
+
+def run_gb300(args, rank, world, local_rank):
+    import torch
+
+    from host_offloaded_kv_gb300.clo import CLOContext
+    from host_offloaded_kv_gb300.synth import Synth
+
+    w = workload_from_args(args)
+    L, B, Hq, Hkv, d, N = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_tokens
+    pool_bytes = L * B * Hkv * N * 4 * d
+    if mem_available_bytes() < pool_bytes * 1.15 + (1 << 30):
+        raise SystemExit(f"not enough host memory for the {pool_bytes / 2**30:.1f} GiB pinned pool of {w.name}")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.Stream(device=dev)
+    syn = Synth(w.seed + 1000 * rank, w.hh_ratio)
+    R = syn.hash_matrices(L, Hkv, d)
+    tau = None if w.tau_fixed is None else np.full(L * Hkv, w.tau_fixed, dtype=np.float32)
+    t0 = time.time()
+    lib = CLOContext(n_layers=L, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, max_tokens=N, hash_R=R,
+                     topk=w.topk, topk_ratio=w.topk_ratio, tau=tau, warmup_steps=w.warmup_steps,
+                     tau_offset=w.tau_offset, n_persist=w.n_persist if tau is None else 0, timing=True,
+                     stream=stream.cuda_stream)
+    Kbuf = np.empty((N, Hkv, d), dtype=np.uint16)
+    Vbuf = np.empty((N, Hkv, d), dtype=np.uint16)
+    for l in range(L):
+        for b in range(B):
+            syn.layer_seq_kv(l, b, Hkv, 0, N, d, Kbuf, Vbuf)
+            lib.append_kv(l, b, Kbuf, Vbuf, src_is_device=False)
+    t_setup = time.time() - t0
+    del Kbuf, Vbuf
+
+    qs = syn.query_stream(L, B, Hq, d, w.rho_lo, w.rho_hi)
+    n_prof = w.warmup_steps if tau is None else 0
+    K, W = args.steps, args.warmup
+    n_dev = n_prof + W + K
+    qdev = torch.empty((n_dev, L, B, Hq, d), dtype=torch.int16, device=dev)
+    qh = np.empty((L, B, Hq, d), dtype=np.uint16)
+    for i in range(n_dev):
+        qs.next(qh)
+        qdev[i].copy_(torch.from_numpy(qh.view(np.int16)))
+    out = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(n_prof + W):
+            lib.decode_step(qdev[i], out)
+    lib.sync()
+    lib.stats()  # drops the per-phase events of untimed steps
+    before = lib.stats()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            lib.decode_step(qdev[n_prof + W + i], out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    st = lib.stats()
+    host_bytes = st["host_bytes"] - before["host_bytes"]
+    hbm_bytes = st["hbm_bytes_alg"] - before["hbm_bytes_alg"]
+    hits = st["units_hit"] - before["units_hit"]
+    miss = st["units_miss"] - before["units_miss"]
+    pers = st["units_persist"] - before["units_persist"]
+    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fetch", "attend")}
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    del qdev
+
+    # end to end through the C ABI with host buffers (pinned): H2D of q, D2H of out per step
+    e2e = None
+    if not args.no_e2e:
+        Ke = K
+        qpin = torch.empty((Ke, L, B, Hq, d), dtype=torch.int16, pin_memory=True)
+        for i in range(Ke):
+            qs.next(qh)
+            qpin[i].copy_(torch.from_numpy(qh.view(np.int16)))
+        opin = torch.empty((L, B, Hq, d), dtype=torch.float32, pin_memory=True)
+        lib.decode_step(qpin[0].numpy(), opin.numpy(), io_on_device=False)
+        lib.stats()
+        if world > 1:
+            torch.distributed.barrier()
+        t1 = time.perf_counter()
+        for i in range(1, Ke):
+            lib.decode_step(qpin[i].numpy(), opin.numpy(), io_on_device=False)
+        t2 = time.perf_counter()
+        lib.stats()
+        sec = t2 - t1
+        if world > 1:
+            t = torch.tensor([sec], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            sec = float(t.item())
+        e2e = {"value": world * B * (Ke - 1) / sec, "unit": UNIT,
+               "h2d_bytes_per_step": L * B * Hq * d * 2, "d2h_bytes_per_step": L * B * Hq * d * 4}
+
+    # pinned host -> device copy bandwidth of this machine (the host-link peak)
+    hb = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        db.copy_(hb, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        db.copy_(hb, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    link_gbs = 5 * (1 << 30) / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del hb, db
+    lib.close()
+
+    hbm_peak, hbm_src = measured_peaks()
+    kmax = topk_of(w)
+    steps = K
+    tokens = world * B * steps
+    value = tokens / (ms_total / 1e3)
+    # algorithmic bytes per phase (per timed region)
+    rec = 4 * d
+    fetch_bytes = host_bytes                       # host -> slot rows (read over the link)
+    attend_hbm = (hits + miss + pers) * kmax * rec + pers * kmax * 4
+    select_hbm = (miss + pers) * (N * 16 + kmax * 4)
+    kern = {}
+    for p in phases:
+        kern[p] = {"ms_per_launch": phases[p] / steps}
+    kern["fetch"].update(bound="host-link", achieved_gbs=fetch_bytes / (phases["fetch"] / 1e3) / 1e9 if phases["fetch"] else None,
+                         peak_gbs=link_gbs)
+    kern["attend"].update(bound="hbm", achieved_gbs=attend_hbm / (phases["attend"] / 1e3) / 1e9, peak_gbs=hbm_peak)
+    kern["select"].update(bound="hbm", achieved_gbs=select_hbm / (phases["select"] / 1e3) / 1e9, peak_gbs=hbm_peak)
+    dom = max(("fetch", "attend", "select"), key=lambda p: phases[p])
+    dk = kern[dom]
+    traffic = traffic_from_profiles(dom, w.name)
+    roofline = {"kernel": {"fetch": "k_gather", "attend": "k_attend", "select": "k_select"}[dom],
+                "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"], "unit": "GB/s",
+                "frac": (dk["achieved_gbs"] / dk["peak_gbs"]) if dk["achieved_gbs"] else None,
+                "traffic": traffic,
+                "peak_source": ("pinned H2D copy measured in this run" if dk["bound"] == "host-link"
+                                else f"MEASURED_PEAKS.json hbm_gbs ({hbm_src})")}
+    step_ideal_ms = max(hbm_bytes / (hbm_peak * 1e9), host_bytes / (link_gbs * 1e9)) * 1e3 / steps
+    step_ms = ms_total / steps
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": W,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded generator; N(0,1) bf16 K/V, 1% heavy hitters, AR(1) queries)",
+        "config": {"workload": w.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
+                   "head_dim": d, "context": N, "topk": kmax, "persistent_heads": w.n_persist if tau is None else 0,
+                   "tau": f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
+                   else w.tau_fixed, "kv_dtype": "bf16", "parallelism": f"replicas x{world} (independent sequences)",
+                   "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
+                         (pool_bytes / 2**30),
+                   "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1)},
+        "gpu_launches": 4 * steps,
+        "roofline": roofline,
+        "step_roofline": {"bound": "max(HBM alg bytes / HBM peak, host bytes / link peak)",
+                          "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,
+                          "hbm_bytes_per_step": hbm_bytes / steps, "host_bytes_per_step": host_bytes / steps,
+                          "link_peak_gbs": link_gbs, "hbm_peak_gbs": hbm_peak},
+        "kernels": kern,
+        "clocks": clocks,
+        "e2e": e2e,
+        "_rank_setup": {"tokens": tokens},
+    }
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+def oracle_sample(args, steps, warm, layers_sampled=1):
+    """Time the CPU oracle on layer 0 of the workload (all sequences and kv heads),
+    scaled to a full step by the layer count."""
+    import oracle as orc
+    from host_offloaded_kv_gb300.synth import Synth
+
+    w = workload_from_args(args)
+    L, B, Hq, Hkv, d, N = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_tokens
+    Ls = layers_sampled
+    syn = Synth(w.seed, w.hh_ratio)
+    R = syn.hash_matrices(L, Hkv, d)[:Ls]
+    tau = None if w.tau_fixed is None else np.full(Ls * Hkv, w.tau_fixed)
+    o = orc.OracleCLO(Ls, B, Hq, Hkv, d, R, topk=w.topk, topk_ratio=w.topk_ratio, tau=tau,
+                      warmup_steps=w.warmup_steps, tau_offset=w.tau_offset,
+                      n_persist=w.n_persist if tau is None else 0, ntok=[N] * B)
+    for l in range(Ls):
+        for b in range(B):
+            for h in range(Hkv):
+                o.set_unit_kv(l, b, h, *syn.unit_kv(l, b, h, 0, N, d))
+    qs = syn.query_stream(L, B, Hq, d, w.rho_lo, w.rho_hi)
+    n_prof = w.warmup_steps if tau is None else 0
+    for _ in range(n_prof + warm):
+        o.step(qs.next()[:Ls])
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        o.step(qs.next()[:Ls])
+    sec = time.perf_counter() - t0
+    per_full_step = sec / steps * (L / Ls)
+    cores = orc.load_oracle().orc_num_threads()
+    return {"value": B / per_full_step, "unit": UNIT, "cores": int(cores), "kind": "oracle",
+            "sample": f"layer 0 of {L} ({Ls * B * Hkv} of {L * B * Hkv} units), {steps} post-profiling steps "
+                      f"after {n_prof} profiling + {warm} warm-up steps; time per step scaled x{L // Ls} to all layers",
+            "seconds_timed": sec}
+
+
+def run_reference(args):
+    import torch
+
+    if torch.cuda.is_available() and not args.no_cpu_baseline:
+        pass
+    K, W = args.steps, args.warmup
+    # bounded: the oracle takes ~0.3-1 s per sampled layer-step; cap the timed steps
+    cb = oracle_sample(args, steps=max(1, min(K, 8)), warm=min(W, 3))
+    w = workload_from_args(args)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 1,
+            "steps": max(1, min(K, 8)), "warmup": min(W, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+            "config": {"workload": w.name}, "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def main():
+    args = parse_args()
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_gb300(args, rank, world, local_rank)
+    line.pop("_rank_setup", None)
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = oracle_sample(args, steps=args.cpu_steps, warm=0)
+        except Exception as e:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"error": str(e)}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

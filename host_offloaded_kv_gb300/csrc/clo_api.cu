@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -69,9 +70,9 @@ struct clo_ctx {
   uint16_t* vstage = nullptr;
   uint16_t* q_io = nullptr;
   float* out_io = nullptr;
-  cudaEvent_t ev[5] = {};
-  bool have_events = false;
-  bool step_timed = false;
+  // per-step phase events (timing mode): 5 markers per step, reused after clo_stats
+  std::vector<std::array<cudaEvent_t, 5>> ev_pool;
+  size_t ev_used = 0;
   uint32_t epoch = 0;
   std::vector<uint8_t> persist_host;  // valid once known
   bool persist_host_valid = false;
@@ -97,9 +98,9 @@ struct clo_ctx {
     pool_host = nullptr;
     if (ntok_pinned) cudaFreeHost(ntok_pinned);
     ntok_pinned = nullptr;
-    if (have_events)
-      for (auto& e : ev) cudaEventDestroy(e);
-    have_events = false;
+    for (auto& set : ev_pool)
+      for (auto& e : set) cudaEventDestroy(e);
+    ev_pool.clear();
   }
 };
 
@@ -259,8 +260,6 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
 
   CLO_TRY(c->dalloc(&c->kstage, (size_t)kStageTokens * c->Hkv * c->d));
   CLO_TRY(c->dalloc(&c->vstage, (size_t)kStageTokens * c->Hkv * c->d));
-  for (auto& ev : c->ev) CLO_CUDA(cudaEventCreate(&ev));
-  c->have_events = true;
   return CLO_OK;
 }
 
@@ -384,23 +383,32 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   DevState& s = c->ds;
   const bool warm = c->warmup_mode && c->step < c->W;
   const bool timed = c->cfg.timing != 0;
+  cudaEvent_t* ev = nullptr;
+  if (timed) {
+    if (c->ev_used == c->ev_pool.size()) {
+      std::array<cudaEvent_t, 5> set{};
+      for (auto& e : set) CLO_CUDA(cudaEventCreate(&e));
+      c->ev_pool.push_back(set);
+    }
+    ev = c->ev_pool[c->ev_used++].data();
+  }
   ++c->epoch;
-  if (timed) CLO_CUDA(cudaEventRecord(c->ev[0], c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[0], c->stream));
   CLO_CUDA(cudaMemsetAsync(s.step_ctr, 0, sizeof(unsigned long long) * C_NUM, c->stream));
   CLO_CUDA(launch_decide(s, qd, c->step, warm ? 1 : 0, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(c->ev[1], c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[1], c->stream));
   CLO_CUDA(launch_select(s, c->sel_cluster, c->sel_chunk, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(c->ev[2], c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
   CLO_CUDA(launch_gather(s, c->epoch, c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[3], c->stream));
   CLO_CUDA(launch_attend(s, qd, od, c->epoch, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(c->ev[3], c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[4], c->stream));
   if (warm && c->step == c->W - 1) {
     CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
     CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
     c->warmup_done = true;
     c->persist_host_valid = false;
   }
-  c->step_timed = timed;
   ++c->step;
   if (!io_on_device) {
     CLO_CUDA(cudaMemcpyAsync(out, c->out_io, sizeof(float) * nq, cudaMemcpyDeviceToHost, c->stream));
@@ -429,12 +437,29 @@ CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
   out->last_host_bytes = (int64_t)last[C_HOST_BYTES];
   out->last_hbm_bytes_alg = (int64_t)last[C_HBM_BYTES];
   out->warmup_done = c->warmup_done ? 1 : 0;
-  if (c->step_timed && c->step > 0) {
-    cudaEventElapsedTime(&out->last_ms_decide, c->ev[0], c->ev[1]);
-    cudaEventElapsedTime(&out->last_ms_select, c->ev[1], c->ev[2]);
-    cudaEventElapsedTime(&out->last_ms_fetch_attend, c->ev[2], c->ev[3]);
-    cudaEventElapsedTime(&out->last_ms_total, c->ev[0], c->ev[3]);
+  out->timed_steps = (int32_t)c->ev_used;
+  for (size_t i = 0; i < c->ev_used; ++i) {
+    const cudaEvent_t* e = c->ev_pool[i].data();
+    float t[5];
+    CLO_CUDA(cudaEventElapsedTime(&t[0], e[0], e[1]));
+    CLO_CUDA(cudaEventElapsedTime(&t[1], e[1], e[2]));
+    CLO_CUDA(cudaEventElapsedTime(&t[2], e[2], e[3]));
+    CLO_CUDA(cudaEventElapsedTime(&t[3], e[3], e[4]));
+    CLO_CUDA(cudaEventElapsedTime(&t[4], e[0], e[4]));
+    out->sum_ms_decide += t[0];
+    out->sum_ms_select += t[1];
+    out->sum_ms_fetch += t[2];
+    out->sum_ms_attend += t[3];
+    out->sum_ms_total += t[4];
+    if (i + 1 == c->ev_used) {
+      out->last_ms_decide = t[0];
+      out->last_ms_select = t[1];
+      out->last_ms_fetch = t[2];
+      out->last_ms_attend = t[3];
+      out->last_ms_total = t[4];
+    }
   }
+  c->ev_used = 0;
   return read_device_error(c);
 }
 
