@@ -25,7 +25,7 @@ _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ER
                  5: "CLO_ERR_STATE", 6: "CLO_ERR_CAPACITY", 7: "CLO_ERR_DEVICE"}
 
 EXPORTED = ["clo_config_default", "clo_init", "clo_destroy", "clo_append_kv", "clo_decode_step", "clo_sync",
-            "clo_stats", "clo_last_error", "clo_debug_get", "clo_set"]
+            "clo_stats", "clo_last_error", "clo_debug_get", "clo_set", "clo_sparse_attention_noalloc"]
 
 
 class CLOError(RuntimeError):
@@ -103,6 +103,8 @@ def load_library(path: str = LIB_PATH):
     lib.clo_debug_get.argtypes = [vp, i32, i32, i32, i32, vp, i64]
     lib.clo_set.restype = ctypes.c_int
     lib.clo_set.argtypes = [vp, i32, i64]
+    lib.clo_sparse_attention_noalloc.restype = ctypes.c_int
+    lib.clo_sparse_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i64, vp]
     _lib = lib
     return lib
 
@@ -180,6 +182,16 @@ def clo_debug_get(ctx, what: int, layer: int, seq: int, kvh: int, dst: np.ndarra
 
 def clo_set(ctx, key: int, value: int) -> None:
     _check(load_library().clo_set(ctx, key, int(value)), "clo_set")
+
+
+def clo_sparse_attention_noalloc(q, rows, out, n_groups: int, group_size: int, head_dim: int, k: int,
+                                 stream=None) -> None:
+    """Allocation-free sparse attention (device buffers; see include/clo.h)."""
+    qp, _ = _ptr(q)
+    rp, _ = _ptr(rows)
+    op, _ = _ptr(out)
+    _check(load_library().clo_sparse_attention_noalloc(qp, rp, op, int(n_groups), int(group_size), int(head_dim),
+                                                       int(k), stream), "clo_sparse_attention_noalloc")
 
 
 # ----------------------------------------------------------------------------- convenience

@@ -541,3 +541,7 @@ CLO_API clo_status clo_set(clo_ctx* c, int32_t key, int64_t value) {
 }
 
 }  // extern "C"
+
+namespace clo {
+void set_last_error_text(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace clo

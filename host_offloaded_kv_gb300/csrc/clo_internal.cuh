@@ -188,3 +188,8 @@ cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64
 size_t select_smem_bytes(int G, int64_t chunk);
 
 }  // namespace clo
+
+namespace clo {
+// Sets the thread-local text returned by clo_last_error().
+void set_last_error_text(const char* msg);
+}  // namespace clo

@@ -198,6 +198,31 @@ CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int3
 enum { CLO_SET_DROP_FLAG_LAYER = 1, CLO_SET_WAIT_TIMEOUT_NS = 2 };
 CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
 
+/* Split-K sparse decode attention that allocates nothing.  The paper has no
+ * counterpart to this call; it is here for callers that are not allowed to
+ * allocate device memory themselves or through the library: a serving engine or
+ * plugin host that plans every byte of device memory up front and hands kernels
+ * only their inputs and outputs, or a latency-critical loop that cannot take the
+ * device-wide stalls cudaMalloc/cudaFree may cause.
+ *   q:    device bf16 [n_groups][group_size][head_dim]  (one GQA group per row)
+ *   rows: device bf16 [n_groups][k][2][head_dim]         (K row then V row of each
+ *         selected token, the layout of the library's cache slots)
+ *   out:  device fp32 [n_groups][group_size][head_dim], written by the call
+ *   out_g = sum_r softmax_r(q_g . K_r / sqrt(head_dim)) V_r over the k rows.
+ * group_size <= 8, head_dim 64 or 128, k >= 1.  Work is enqueued on stream
+ * (cudaStream_t, NULL = legacy default stream) and the call returns at once.
+ * Scratch: one fixed array of about 8 MiB in device memory, defined in the
+ * library and held by every GPU that loads it until the process exits.  Sizes
+ * beyond it are rejected with CLO_ERR_INVALID: n_groups <= 4096 and
+ * n_groups * ceil(k / 256) * group_size * (head_dim + 2) <= 2097152.
+ * The first call on a device looks up that array's device address (once per
+ * device, with that device current); make the first call before any stream
+ * capture.  All calls share the array: calls whose work overlaps on the GPU race
+ * on it, so serialise them (one stream, or events).  No cudaMalloc, cudaFree or
+ * other allocating routine is called.  Errors: CLO_ERR_INVALID, CLO_ERR_CUDA. */
+CLO_API clo_status clo_sparse_attention_noalloc(const void* q, const void* rows, float* out, int32_t n_groups,
+                                                int32_t group_size, int32_t head_dim, int64_t k, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
