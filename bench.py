@@ -229,7 +229,7 @@ def run_gb300(args, rank, world, local_rank):
     hits = st["units_hit"] - before["units_hit"]
     miss = st["units_miss"] - before["units_miss"]
     pers = st["units_persist"] - before["units_persist"]
-    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fetch", "attend")}
+    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fetch_attend")}
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -292,14 +292,16 @@ def run_gb300(args, rank, world, local_rank):
     kern = {}
     for p in phases:
         kern[p] = {"ms_per_launch": phases[p] / steps}
-    kern["fetch"].update(bound="host-link", achieved_gbs=fetch_bytes / (phases["fetch"] / 1e3) / 1e9 if phases["fetch"] else None,
-                         peak_gbs=link_gbs)
-    kern["attend"].update(bound="hbm", achieved_gbs=attend_hbm / (phases["attend"] / 1e3) / 1e9, peak_gbs=hbm_peak)
+    fa_s = phases["fetch_attend"] / 1e3
+    kern["fetch_attend"].update(
+        bound="host-link", achieved_gbs=fetch_bytes / fa_s / 1e9 if fetch_bytes else 0.0, peak_gbs=link_gbs,
+        hbm_gbs=(attend_hbm + fetch_bytes) / fa_s / 1e9,
+        note="host bytes over the link / kernel time; hbm_gbs = attention row reads + slot writes / kernel time")
     kern["select"].update(bound="hbm", achieved_gbs=select_hbm / (phases["select"] / 1e3) / 1e9, peak_gbs=hbm_peak)
-    dom = max(("fetch", "attend", "select"), key=lambda p: phases[p])
+    dom = max(("fetch_attend", "select"), key=lambda p: phases[p])
     dk = kern[dom]
     traffic = traffic_from_profiles(dom, w.name)
-    roofline = {"kernel": {"fetch": "k_gather", "attend": "k_attend", "select": "k_select"}[dom],
+    roofline = {"kernel": {"fetch_attend": "k_fetch_attend", "select": "k_select"}[dom],
                 "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"], "unit": "GB/s",
                 "frac": (dk["achieved_gbs"] / dk["peak_gbs"]) if dk["achieved_gbs"] else None,
                 "traffic": traffic,
@@ -318,7 +320,7 @@ def run_gb300(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1)},
-        "gpu_launches": 4 * steps,
+        "gpu_launches": 3 * steps,
         "roofline": roofline,
         "step_roofline": {"bound": "max(HBM alg bytes / HBM peak, host bytes / link peak)",
                           "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,

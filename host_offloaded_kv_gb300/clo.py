@@ -62,10 +62,9 @@ class clo_stats_t(ctypes.Structure):
         "steps", "units_hit", "units_miss", "units_persist", "host_bytes", "hbm_bytes_alg", "timeouts",
         "last_hit", "last_miss", "last_persist", "last_host_bytes", "last_hbm_bytes_alg")] + \
         [("warmup_done", ctypes.c_int32), ("timed_steps", ctypes.c_int32)] + \
-        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_select", "last_ms_fetch", "last_ms_attend",
+        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_select", "last_ms_fetch_attend",
                                        "last_ms_total")] + \
-        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_select", "sum_ms_fetch", "sum_ms_attend",
-                                        "sum_ms_total")]
+        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_select", "sum_ms_fetch_attend", "sum_ms_total")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

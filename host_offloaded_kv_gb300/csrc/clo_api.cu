@@ -70,10 +70,12 @@ struct clo_ctx {
   uint16_t* vstage = nullptr;
   uint16_t* q_io = nullptr;
   float* out_io = nullptr;
-  // per-step phase events (timing mode): 5 markers per step, reused after clo_stats
-  std::vector<std::array<cudaEvent_t, 5>> ev_pool;
+  // per-step phase events (timing mode): 4 markers per step, reused after clo_stats
+  std::vector<std::array<cudaEvent_t, 4>> ev_pool;
   size_t ev_used = 0;
   uint32_t epoch = 0;
+  uint32_t* step_zero = nullptr;  // zeroed at the start of every step
+  size_t step_zero_bytes = 0;
   std::vector<uint8_t> persist_host;  // valid once known
   bool persist_host_valid = false;
 
@@ -231,11 +233,23 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   } else {
     s.resident = nullptr;
   }
-  CLO_TRY(c->dalloc(&s.step_ctr, (size_t)C_NUM));
+  // per-step zeroed region: step counters, per-layer list counts, work queues, ready flags
+  {
+    const size_t words = 2 * (size_t)C_NUM + 2 * (size_t)c->L + 4 + (size_t)U * s.nsplit;
+    uint32_t* z = nullptr;
+    CLO_TRY(c->dalloc(&z, words));
+    c->step_zero = z;
+    c->step_zero_bytes = words * sizeof(uint32_t);
+    s.step_ctr = reinterpret_cast<unsigned long long*>(z);
+    s.lcnt = reinterpret_cast<int*>(z + 2 * C_NUM);
+    s.queue = z + 2 * C_NUM + 2 * c->L;
+    s.ready = z + 2 * C_NUM + 2 * c->L + 4;
+  }
+  CLO_TRY(c->dalloc(&s.other_list, (size_t)c->L * c->B * c->Hkv));
+  CLO_TRY(c->dalloc(&s.miss_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM));
   CLO_TRY(c->dalloc(&s.err, 1));
   CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));
-  CLO_TRY(c->dalloc(&s.ready, (size_t)U));
   CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * c->G * (c->d + 2)));
 
   std::vector<int32_t> pslot((size_t)LH, -1);
@@ -386,7 +400,7 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   cudaEvent_t* ev = nullptr;
   if (timed) {
     if (c->ev_used == c->ev_pool.size()) {
-      std::array<cudaEvent_t, 5> set{};
+      std::array<cudaEvent_t, 4> set{};
       for (auto& e : set) CLO_CUDA(cudaEventCreate(&e));
       c->ev_pool.push_back(set);
     }
@@ -394,15 +408,13 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   }
   ++c->epoch;
   if (timed) CLO_CUDA(cudaEventRecord(ev[0], c->stream));
-  CLO_CUDA(cudaMemsetAsync(s.step_ctr, 0, sizeof(unsigned long long) * C_NUM, c->stream));
+  CLO_CUDA(cudaMemsetAsync(c->step_zero, 0, c->step_zero_bytes, c->stream));
   CLO_CUDA(launch_decide(s, qd, c->step, warm ? 1 : 0, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[1], c->stream));
   CLO_CUDA(launch_select(s, c->sel_cluster, c->sel_chunk, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
-  CLO_CUDA(launch_gather(s, c->epoch, c->stream));
+  CLO_CUDA(launch_fetch_attend(s, qd, od, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[3], c->stream));
-  CLO_CUDA(launch_attend(s, qd, od, c->epoch, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(ev[4], c->stream));
   if (warm && c->step == c->W - 1) {
     CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
     CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
@@ -440,23 +452,20 @@ CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
   out->timed_steps = (int32_t)c->ev_used;
   for (size_t i = 0; i < c->ev_used; ++i) {
     const cudaEvent_t* e = c->ev_pool[i].data();
-    float t[5];
+    float t[4];
     CLO_CUDA(cudaEventElapsedTime(&t[0], e[0], e[1]));
     CLO_CUDA(cudaEventElapsedTime(&t[1], e[1], e[2]));
     CLO_CUDA(cudaEventElapsedTime(&t[2], e[2], e[3]));
-    CLO_CUDA(cudaEventElapsedTime(&t[3], e[3], e[4]));
-    CLO_CUDA(cudaEventElapsedTime(&t[4], e[0], e[4]));
+    CLO_CUDA(cudaEventElapsedTime(&t[3], e[0], e[3]));
     out->sum_ms_decide += t[0];
     out->sum_ms_select += t[1];
-    out->sum_ms_fetch += t[2];
-    out->sum_ms_attend += t[3];
-    out->sum_ms_total += t[4];
+    out->sum_ms_fetch_attend += t[2];
+    out->sum_ms_total += t[3];
     if (i + 1 == c->ev_used) {
       out->last_ms_decide = t[0];
       out->last_ms_select = t[1];
-      out->last_ms_fetch = t[2];
-      out->last_ms_attend = t[3];
-      out->last_ms_total = t[4];
+      out->last_ms_fetch_attend = t[2];
+      out->last_ms_total = t[3];
     }
   }
   c->ev_used = 0;

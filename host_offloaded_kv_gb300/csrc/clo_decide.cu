@@ -87,6 +87,12 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
     s.decision[u] = (uint8_t)dec;
     s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
     s_dec = dec;
+    // per-layer work lists of the fused fetch/attention kernel
+    const int BH = s.B * s.Hkv;
+    if (dec == CLO_DEC_MISS)
+      s.miss_list[(int64_t)l * BH + atomicAdd(&s.lcnt[s.L + l], 1)] = (int32_t)u;
+    else
+      s.other_list[(int64_t)l * BH + atomicAdd(&s.lcnt[l], 1)] = (int32_t)u;
 
     // counters: decisions, host bytes, algorithmic HBM bytes of this unit's step
     const int64_t N = s.ntok[b];

@@ -66,10 +66,16 @@ struct DevState {
   float* part;                  // attention partials [U][nsplit][G][d + 2]
   int nsplit;                   // attention splits per unit
   int split_rows;               // rows per split
-  uint32_t* ready;              // [U] fetch-ready epochs
+  uint32_t* ready;              // [U][nsplit] fetch-ready flag per row chunk (zeroed per step)
+  int* lcnt;                    // [2L] per-layer counts: other units [L], missed units [L] (zeroed per step)
+  int32_t* other_list;          // [L][B*Hkv] reused and persistent units of each layer
+  int32_t* miss_list;           // [L][B*Hkv] missed units of each layer
+  unsigned* queue;              // [2] work counters: fetch, attention (zeroed per step)
   int64_t wait_timeout_ns;
   int drop_flag_layer;
 };
+
+constexpr int kMaxLayers = 256;
 
 __host__ __device__ inline int64_t unit_of(const DevState& s, int l, int b, int h) {
   return ((int64_t)l * s.B + b) * s.Hkv + h;
@@ -179,8 +185,7 @@ cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_
 cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st);
 cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st);
 cudaError_t launch_select(const DevState& s, int cluster, int64_t chunk, cudaStream_t st);
-cudaError_t launch_gather(const DevState& s, uint32_t epoch, cudaStream_t st);
-cudaError_t launch_attend(const DevState& s, const uint16_t* q, float* out, uint32_t epoch, cudaStream_t st);
+cudaError_t launch_fetch_attend(const DevState& s, const uint16_t* q, float* out, cudaStream_t st);
 cudaError_t launch_resident_fill(const DevState& s, int64_t t0, int64_t t1, cudaStream_t st);
 cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
                               const uint16_t* vdev, cudaStream_t st);

@@ -111,12 +111,12 @@ typedef struct clo_stats_t {
   int64_t last_hit, last_miss, last_persist, last_host_bytes, last_hbm_bytes_alg;
   int32_t warmup_done;       /* 1 once thresholds and persistent heads are fixed */
   /* timing != 0: CUDA-event times of the phases (decide = reuse test and query
-   * hashing, select = scoring and top-k, fetch = host-row gather, attend = sparse
-   * attention, total = whole step), for the last step and summed over the
+   * hashing, select = scoring and top-k, fetch_attend = host-row fetch fused with
+   * sparse attention, total = whole step), for the last step and summed over the
    * timed_steps steps since the previous clo_stats call. */
   int32_t timed_steps;
-  float last_ms_decide, last_ms_select, last_ms_fetch, last_ms_attend, last_ms_total;
-  double sum_ms_decide, sum_ms_select, sum_ms_fetch, sum_ms_attend, sum_ms_total;
+  float last_ms_decide, last_ms_select, last_ms_fetch_attend, last_ms_total;
+  double sum_ms_decide, sum_ms_select, sum_ms_fetch_attend, sum_ms_total;
 } clo_stats_t;
 
 /* Fill *cfg with defaults (shapes zero; topk_ratio 0.1; warmup_steps 16;
