@@ -134,11 +134,30 @@ def traffic_from_profiles(kernel: str, workload: str):
         if line.startswith("traffic_bytes_per_launch:"):
             val = line.split(":", 1)[1].strip()
             traffic = None if val in ("", "null") else float(val)
-    src = os.path.join(ROOT, "host_offloaded_kv_gb300", "csrc", "clo_attend.cu")
+    src = os.path.join(ROOT, "host_offloaded_kv_gb300", "csrc", "clo_fused.cu")
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if want != digest:
         return None
     return traffic
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank's time); identity for one rank.
+    Works with the gloo (CPU tensors) and nccl (CUDA tensors) backends."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, seconds_slowest: float, world: int) -> float:
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    return world * units_per_rank / seconds_slowest
 
 
 # ----------------------------------------------------------------------------- workload
@@ -224,16 +243,16 @@ def run_gb300(args, rank, world, local_rank):
     clocks = sampler.stop()
     ms_total = ev0.elapsed_time(ev1)
     st = lib.stats()
+    timeline = lib.timeline()
+    if timeline is not None:
+        timeline["host_bytes"] = st["last_host_bytes"]
     host_bytes = st["host_bytes"] - before["host_bytes"]
     hbm_bytes = st["hbm_bytes_alg"] - before["hbm_bytes_alg"]
     hits = st["units_hit"] - before["units_hit"]
     miss = st["units_miss"] - before["units_miss"]
     pers = st["units_persist"] - before["units_persist"]
-    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fetch_attend")}
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fused")}
+    ms_total = max_over_ranks(ms_total, world)
     del qdev
 
     # end to end through the C ABI with host buffers (pinned): H2D of q, D2H of out per step
@@ -254,12 +273,8 @@ def run_gb300(args, rank, world, local_rank):
             lib.decode_step(qpin[i].numpy(), opin.numpy(), io_on_device=False)
         t2 = time.perf_counter()
         lib.stats()
-        sec = t2 - t1
-        if world > 1:
-            t = torch.tensor([sec], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            sec = float(t.item())
-        e2e = {"value": world * B * (Ke - 1) / sec, "unit": UNIT,
+        sec = max_over_ranks(t2 - t1, world)
+        e2e = {"value": whole_job_rate(B * (Ke - 1), sec, world), "unit": UNIT,
                "h2d_bytes_per_step": L * B * Hq * d * 2, "d2h_bytes_per_step": L * B * Hq * d * 4}
 
     # pinned host -> device copy bandwidth of this machine (the host-link peak)
@@ -283,7 +298,7 @@ def run_gb300(args, rank, world, local_rank):
     kmax = topk_of(w)
     steps = K
     tokens = world * B * steps
-    value = tokens / (ms_total / 1e3)
+    value = whole_job_rate(B * steps, ms_total / 1e3, world)
     # algorithmic bytes per phase (per timed region)
     rec = 4 * d
     fetch_bytes = host_bytes                       # host -> slot rows (read over the link)
@@ -292,16 +307,19 @@ def run_gb300(args, rank, world, local_rank):
     kern = {}
     for p in phases:
         kern[p] = {"ms_per_launch": phases[p] / steps}
-    fa_s = phases["fetch_attend"] / 1e3
-    kern["fetch_attend"].update(
-        bound="host-link", achieved_gbs=fetch_bytes / fa_s / 1e9 if fetch_bytes else 0.0, peak_gbs=link_gbs,
-        hbm_gbs=(attend_hbm + fetch_bytes) / fa_s / 1e9,
-        note="host bytes over the link / kernel time; hbm_gbs = attention row reads + slot writes / kernel time")
-    kern["select"].update(bound="hbm", achieved_gbs=select_hbm / (phases["select"] / 1e3) / 1e9, peak_gbs=hbm_peak)
-    dom = max(("fetch_attend", "select"), key=lambda p: phases[p])
+    fu_s = phases["fused"] / 1e3
+    kern["fused"].update(
+        bound="host-link", achieved_gbs=fetch_bytes / fu_s / 1e9 if fetch_bytes else 0.0, peak_gbs=link_gbs,
+        hbm_gbs=(attend_hbm + fetch_bytes + pers * (N * 16 + kmax * 4)) / fu_s / 1e9,
+        note="host bytes over the link / kernel time; hbm_gbs = (code reads of the persistent units' selections "
+             "+ attention row reads + slot writes) / kernel time")
+    sel_s = phases["select"] / 1e3
+    kern["select"].update(bound="hbm", achieved_gbs=miss * (N * 16 + kmax * 4) / sel_s / 1e9 if sel_s else None,
+                          peak_gbs=hbm_peak, note="code reads + index writes of the missed units' selections")
+    dom = "fused"
     dk = kern[dom]
     traffic = traffic_from_profiles(dom, w.name)
-    roofline = {"kernel": {"fetch_attend": "k_fetch_attend", "select": "k_select"}[dom],
+    roofline = {"kernel": "k_step_fused",
                 "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"], "unit": "GB/s",
                 "frac": (dk["achieved_gbs"] / dk["peak_gbs"]) if dk["achieved_gbs"] else None,
                 "traffic": traffic,
@@ -328,6 +346,7 @@ def run_gb300(args, rank, world, local_rank):
                           "link_peak_gbs": link_gbs, "hbm_peak_gbs": hbm_peak},
         "kernels": kern,
         "clocks": clocks,
+        "timeline_last_step": timeline,
         "e2e": e2e,
         "_rank_setup": {"tokens": tokens},
     }

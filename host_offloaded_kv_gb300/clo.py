@@ -18,7 +18,7 @@ CLO_OK, CLO_ERR_INVALID, CLO_ERR_OOM, CLO_ERR_CUDA, CLO_ERR_TIMEOUT, CLO_ERR_STA
     CLO_ERR_DEVICE = range(8)
 CLO_DEC_HIT, CLO_DEC_MISS, CLO_DEC_PERSIST = 0, 1, 2
 (CLO_DBG_KEY_CODES, CLO_DBG_QUERY_CODES, CLO_DBG_IDX, CLO_DBG_DECISION, CLO_DBG_SLOT_ROWS, CLO_DBG_TAU,
- CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS) = range(1, 10)
+ CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS, CLO_DBG_TIMELINE) = range(1, 11)
 CLO_SET_DROP_FLAG_LAYER, CLO_SET_WAIT_TIMEOUT_NS = 1, 2
 
 _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ERR_CUDA", 4: "CLO_ERR_TIMEOUT",
@@ -62,9 +62,8 @@ class clo_stats_t(ctypes.Structure):
         "steps", "units_hit", "units_miss", "units_persist", "host_bytes", "hbm_bytes_alg", "timeouts",
         "last_hit", "last_miss", "last_persist", "last_host_bytes", "last_hbm_bytes_alg")] + \
         [("warmup_done", ctypes.c_int32), ("timed_steps", ctypes.c_int32)] + \
-        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_select", "last_ms_fetch_attend",
-                                       "last_ms_total")] + \
-        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_select", "sum_ms_fetch_attend", "sum_ms_total")]
+        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_select", "last_ms_fused", "last_ms_total")] + \
+        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_select", "sum_ms_fused", "sum_ms_total")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -291,3 +290,14 @@ class CLOContext:
 
     def shat(self):
         return clo_debug_get(self.ctx, CLO_DBG_SHAT, 0, 0, 0, np.empty((self.L, self.Hkv), dtype=np.float64))
+
+    def timeline(self):
+        """Stamps of the last step's fused kernel (timing mode), in us from its start."""
+        t = clo_debug_get(self.ctx, CLO_DBG_TIMELINE, 0, 0, 0, np.empty(16, dtype=np.uint64)).astype(np.int64)
+        if t[0] == 0:
+            return None
+        rel = lambda v: None if v == 0 else round((int(v) - int(t[0])) / 1e3, 1)  # noqa: E731
+        return {"sel_missed_done_us": rel(t[1]), "sel_persistent_done_us": rel(t[2]),
+                "first_fetch_us": rel(t[3]), "fetch_done_us": rel(t[4]), "first_attention_us": rel(t[5]),
+                "attention_done_us": rel(t[6]), "fetch_wait_sum_us": round(int(t[7]) / 1e3, 1),
+                "attention_wait_sum_us": round(int(t[8]) / 1e3, 1)}

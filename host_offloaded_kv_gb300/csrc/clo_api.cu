@@ -36,9 +36,8 @@ clo_status fail(clo_status st, const std::string& msg) {
   } while (0)
 
 constexpr int kSplitRows = 256;
-constexpr int64_t kSelTargetChunk = 16384;
-constexpr int64_t kSelTile = 512;
 constexpr int64_t kStageTokens = 16384;
+constexpr int64_t kSelClusterChunk = 16384;
 
 int64_t topk_for(int64_t N, int64_t topk, double ratio) {
   if (N <= 0) return 0;
@@ -76,6 +75,7 @@ struct clo_ctx {
   uint32_t epoch = 0;
   uint32_t* step_zero = nullptr;  // zeroed at the start of every step
   size_t step_zero_bytes = 0;
+  unsigned long long* timeline_dev = nullptr;  // inside step_zero
   std::vector<uint8_t> persist_host;  // valid once known
   bool persist_host_valid = false;
 
@@ -233,21 +233,43 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   } else {
     s.resident = nullptr;
   }
-  // per-step zeroed region: step counters, per-layer list counts, work queues, ready flags
+  // per-step zeroed region: step counters, per-layer list lengths, work queues, ready
+  // flags of the fetch chunks, selection progress counters
+  s.nch = (int)((c->Nmax + kSelChunk - 1) / kSelChunk);
+  s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
   {
-    const size_t words = 2 * (size_t)C_NUM + 2 * (size_t)c->L + 4 + (size_t)U * s.nsplit;
+    size_t off = 2 * (size_t)C_NUM * kCtrLanes;
+    const size_t o_lcnt = off;
+    off += 3 * (size_t)c->L;
+    const size_t o_queue = off;
+    off += 4;
+    const size_t o_ready = off;
+    off += (size_t)U * s.nsplit;
+    const size_t o_sel = off;
+    off += 3 * (size_t)U;
+    off = (off + 1) / 2 * 2;  // 8-byte alignment for the timeline
+    const size_t o_tl = off;
+    off += 2 * (size_t)kTimelineSlots;
     uint32_t* z = nullptr;
-    CLO_TRY(c->dalloc(&z, words));
+    CLO_TRY(c->dalloc(&z, off));
     c->step_zero = z;
-    c->step_zero_bytes = words * sizeof(uint32_t);
+    c->step_zero_bytes = off * sizeof(uint32_t);
     s.step_ctr = reinterpret_cast<unsigned long long*>(z);
-    s.lcnt = reinterpret_cast<int*>(z + 2 * C_NUM);
-    s.queue = z + 2 * C_NUM + 2 * c->L;
-    s.ready = z + 2 * C_NUM + 2 * c->L + 4;
+    s.lcnt = reinterpret_cast<int*>(z + o_lcnt);
+    s.queue = z + o_queue;
+    s.ready = z + o_ready;
+    s.score_done = z + o_sel;
+    s.fin_done = z + o_sel + U;
+    s.sel_cnt = z + o_sel + 2 * U;
+    c->timeline_dev = reinterpret_cast<unsigned long long*>(z + o_tl);
+    s.timeline = cfg->timing ? c->timeline_dev : nullptr;
   }
-  CLO_TRY(c->dalloc(&s.other_list, (size_t)c->L * c->B * c->Hkv));
+  CLO_TRY(c->dalloc(&s.hit_list, (size_t)c->L * c->B * c->Hkv));
+  CLO_TRY(c->dalloc(&s.pers_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.miss_list, (size_t)c->L * c->B * c->Hkv));
-  CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM));
+  CLO_TRY(c->dalloc(&s.sel_hist, (size_t)U * s.nch * s.nbp));
+  CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * s.nch));
+  CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
   CLO_TRY(c->dalloc(&s.err, 1));
   CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));
   CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * c->G * (c->d + 2)));
@@ -367,11 +389,11 @@ static clo_status refresh_lengths(clo_ctx* c) {
   CLO_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(c->ds.kcount), kc, sizeof(int32_t) * c->B, cudaMemcpyHostToDevice,
                            c->stream));
   CLO_CUDA(cudaStreamSynchronize(c->stream));  // the pinned staging is reused
-  // cluster of CTAs per unit for the selection: chunks of about 16K tokens, <= 8 CTAs
+  // selection of missed units: a cluster of CTAs per unit, chunks of <= 16K tokens
   int C = 1;
-  while (C < 8 && (nmax + C - 1) / C > kSelTargetChunk) C *= 2;
+  while (C < 8 && (nmax + C - 1) / C > kSelClusterChunk) C *= 2;
   int64_t chunk = (nmax + C - 1) / C;
-  chunk = (chunk + kSelTile - 1) / kSelTile * kSelTile;
+  chunk = (chunk + 511) / 512 * 512;
   c->sel_cluster = C;
   c->sel_chunk = chunk;
   c->ntok_dirty = false;
@@ -413,7 +435,7 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   if (timed) CLO_CUDA(cudaEventRecord(ev[1], c->stream));
   CLO_CUDA(launch_select(s, c->sel_cluster, c->sel_chunk, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
-  CLO_CUDA(launch_fetch_attend(s, qd, od, c->stream));
+  CLO_CUDA(launch_step_fused(s, qd, od, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[3], c->stream));
   if (warm && c->step == c->W - 1) {
     CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
@@ -432,9 +454,13 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
 CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
   if (!c || !out) return fail(CLO_ERR_INVALID, "null argument");
   CLO_CUDA(cudaStreamSynchronize(c->stream));
-  unsigned long long last[C_NUM], tot[C_NUM];
-  CLO_CUDA(cudaMemcpy(last, c->ds.step_ctr, sizeof(last), cudaMemcpyDeviceToHost));
-  CLO_CUDA(cudaMemcpy(tot, c->ds.total_ctr, sizeof(tot), cudaMemcpyDeviceToHost));
+  unsigned long long last_l[C_NUM * kCtrLanes], tot_l[C_NUM * kCtrLanes], last[C_NUM] = {}, tot[C_NUM] = {};
+  CLO_CUDA(cudaMemcpy(last_l, c->ds.step_ctr, sizeof(last_l), cudaMemcpyDeviceToHost));
+  CLO_CUDA(cudaMemcpy(tot_l, c->ds.total_ctr, sizeof(tot_l), cudaMemcpyDeviceToHost));
+  for (int i = 0; i < C_NUM * kCtrLanes; ++i) {
+    last[i / kCtrLanes] += last_l[i];
+    tot[i / kCtrLanes] += tot_l[i];
+  }
   std::memset(out, 0, sizeof(*out));
   out->steps = c->step;
   out->units_hit = (int64_t)tot[C_HIT];
@@ -459,12 +485,12 @@ CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
     CLO_CUDA(cudaEventElapsedTime(&t[3], e[0], e[3]));
     out->sum_ms_decide += t[0];
     out->sum_ms_select += t[1];
-    out->sum_ms_fetch_attend += t[2];
+    out->sum_ms_fused += t[2];
     out->sum_ms_total += t[3];
     if (i + 1 == c->ev_used) {
       out->last_ms_decide = t[0];
       out->last_ms_select = t[1];
-      out->last_ms_fetch_attend = t[2];
+      out->last_ms_fused = t[2];
       out->last_ms_total = t[3];
     }
   }
@@ -522,6 +548,10 @@ CLO_API clo_status clo_debug_get(clo_ctx* c, int32_t what, int32_t layer, int32_
     case CLO_DBG_COS:
       src = s.cosv;
       bytes = c->U * 4;
+      break;
+    case CLO_DBG_TIMELINE:
+      src = c->timeline_dev;
+      bytes = (int64_t)kTimelineSlots * 8;
       break;
     default:
       return fail(CLO_ERR_INVALID, "unknown debug item " + std::to_string(what));

@@ -18,6 +18,11 @@ namespace {
 
 constexpr int kDecideThreads = 128;
 
+
+__device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, int64_t step, int warmup_active, int l,
+                            int b, int h, const uint16_t* Rs, float* qs, float (*red)[kDecideThreads / 32],
+                            int* s_dec_p, uint32_t (*words)[4]);
+
 struct StridedF32 {
   const float* p;
   int stride;
@@ -29,8 +34,12 @@ struct StridedBF16 {
   __device__ float operator()(int i) const { return bf16_bits_to_f32(p[i * stride]); }
 };
 
+// One CTA per unit; the head's projection R (d x 128 bf16) is staged in shared
+// memory with asynchronous 16-byte copies issued together, overlapping the
+// cosine of the reuse test.
 __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uint16_t* __restrict__ q, int64_t step,
                                                             int warmup_active) {
+  __shared__ __align__(16) uint16_t Rs[kMaxD * 128];
   __shared__ float qs[kMaxG * kMaxD];
   __shared__ float red[3][kDecideThreads / 32];
   __shared__ int s_dec;
@@ -40,6 +49,19 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
   const int l = (int)(u / ((int64_t)s.Hkv * s.B));
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(s.R + ((int64_t)l * s.Hkv + h) * s.d * 128);
+    for (int e = threadIdx.x; e < s.d * 128 / 8; e += kDecideThreads) cp_async16(&Rs[e * 8], src + e);
+    cp_async_commit();
+  }
+  decide_unit(s, q, step, warmup_active, l, b, h, Rs, qs, red, &s_dec, words);
+}
+
+__device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, int64_t step, int warmup_active, int l,
+                            int b, int h, const uint16_t* Rs, float* qs, float (*red)[kDecideThreads / 32],
+                            int* s_dec_p, uint32_t (*words)[4]) {
+  int& s_dec = *s_dec_p;
+  const int64_t u = unit_of(s, l, b, h);
   const int G = s.G, d = s.d, GD = s.G * s.d;
   const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * d;
   uint16_t* qc = s.qcache + u * GD;
@@ -87,12 +109,11 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
     s.decision[u] = (uint8_t)dec;
     s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
     s_dec = dec;
-    // per-layer work lists of the fused fetch/attention kernel
+    // per-layer work lists of the fused step kernel: hit, persistent, missed
     const int BH = s.B * s.Hkv;
-    if (dec == CLO_DEC_MISS)
-      s.miss_list[(int64_t)l * BH + atomicAdd(&s.lcnt[s.L + l], 1)] = (int32_t)u;
-    else
-      s.other_list[(int64_t)l * BH + atomicAdd(&s.lcnt[l], 1)] = (int32_t)u;
+    const int li = dec == CLO_DEC_HIT ? 0 : (dec == CLO_DEC_PERSIST ? 1 : 2);
+    int32_t* lst = li == 0 ? s.hit_list : (li == 1 ? s.pers_list : s.miss_list);
+    lst[(int64_t)l * BH + atomicAdd(&s.lcnt[li * s.L + l], 1)] = (int32_t)u;
 
     // counters: decisions, host bytes, algorithmic HBM bytes of this unit's step
     const int64_t N = s.ntok[b];
@@ -104,14 +125,14 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
     if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
     if (dec == CLO_DEC_PERSIST) hbm += k * 4;
     const int slot = dec == CLO_DEC_HIT ? C_HIT : (dec == CLO_DEC_MISS ? C_MISS : C_PERSIST);
-    atomicAdd(&s.step_ctr[slot], 1ull);
-    atomicAdd(&s.total_ctr[slot], 1ull);
+    atomicAdd(&s.step_ctr[ctr_at(slot, u)], 1ull);
+    atomicAdd(&s.total_ctr[ctr_at(slot, u)], 1ull);
     if (host) {
-      atomicAdd(&s.step_ctr[C_HOST_BYTES], host);
-      atomicAdd(&s.total_ctr[C_HOST_BYTES], host);
+      atomicAdd(&s.step_ctr[ctr_at(C_HOST_BYTES, u)], host);
+      atomicAdd(&s.total_ctr[ctr_at(C_HOST_BYTES, u)], host);
     }
-    atomicAdd(&s.step_ctr[C_HBM_BYTES], (unsigned long long)hbm);
-    atomicAdd(&s.total_ctr[C_HBM_BYTES], (unsigned long long)hbm);
+    atomicAdd(&s.step_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
+    atomicAdd(&s.total_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
   }
   __syncthreads();
   const int dec = s_dec;
@@ -119,14 +140,17 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
     for (int e = threadIdx.x; e < GD; e += kDecideThreads) qc[e] = qg[e];
     if (threadIdx.x == 0) s.qvalid[u] = 1;
   }
-  if (dec == CLO_DEC_HIT) return;
+  cp_async_wait<0>();  // R staged (also before any exit: no copy may outlive the CTA)
+  __syncthreads();
+  if (dec == CLO_DEC_HIT) return;  // uniform over the CTA
 
   // query codes of the G heads: thread j computes bit j of every head
   const int j = threadIdx.x;  // 128 threads = 128 bits
-  const uint16_t* Rg = s.R + ((int64_t)l * s.Hkv + h) * d * 128;
+  const uint16_t* Rg = Rs;
   float acc[kMaxG], aab[kMaxG];
 #pragma unroll
   for (int g = 0; g < kMaxG; ++g) acc[g] = aab[g] = 0.f;
+#pragma unroll 4
   for (int i = 0; i < d; ++i) {
     const float r = bf16_bits_to_f32(Rg[i * 128 + j]);
 #pragma unroll

@@ -36,6 +36,11 @@ enum Counter : int {
   C_TIMEOUTS = 5,
   C_NUM = 8
 };
+// each counter is spread over kCtrLanes addresses (by unit) to keep atomics uncontended
+constexpr int kCtrLanes = 32;
+__host__ __device__ inline int ctr_at(int counter, int64_t unit) {
+  return counter * kCtrLanes + (int)(unit & (kCtrLanes - 1));
+}
 
 struct DevState {
   int L, B, Hq, Hkv, d, G;
@@ -59,23 +64,48 @@ struct DevState {
   uint16_t* slots;              // [U][kmax][2d]
   uint16_t* resident;           // [L][B][P][Nmax][2d]
   const uint16_t* pool;         // device view of the host pool [U][Nmax][2d]
-  unsigned long long* step_ctr; // [C_NUM] this step
-  unsigned long long* total_ctr;// [C_NUM] since init
+  unsigned long long* step_ctr; // [C_NUM][kCtrLanes] this step (summed by the host)
+  unsigned long long* total_ctr;// [C_NUM][kCtrLanes] since init
   uint32_t* err;                // error word
   uint32_t* unit_done;          // [U] split counters of the attention combine
   float* part;                  // attention partials [U][nsplit][G][d + 2]
   int nsplit;                   // attention splits per unit
   int split_rows;               // rows per split
   uint32_t* ready;              // [U][nsplit] fetch-ready flag per row chunk (zeroed per step)
-  int* lcnt;                    // [2L] per-layer counts: other units [L], missed units [L] (zeroed per step)
-  int32_t* other_list;          // [L][B*Hkv] reused and persistent units of each layer
-  int32_t* miss_list;           // [L][B*Hkv] missed units of each layer
-  unsigned* queue;              // [2] work counters: fetch, attention (zeroed per step)
+  int* lcnt;                    // [3L] per-layer list lengths: hit, persistent, missed (zeroed per step)
+  int32_t* hit_list;            // [L][B*Hkv] units reusing their selection, per layer
+  int32_t* pers_list;           // [L][B*Hkv] persistent units, per layer
+  int32_t* miss_list;           // [L][B*Hkv] missed units, per layer
+  unsigned* queue;              // [2] work counters: fetch, compute (zeroed per step)
+  uint32_t* sel_hist;           // [U][nch][nbp] score histogram of each selection chunk
+  int4* sel_meta;               // [U][nch] {output offset, tie quota, threshold T, 0}
+  uint32_t* score_done;         // [U] chunks scored (zeroed per step)
+  uint32_t* fin_done;           // [U] threshold known (zeroed per step)
+  uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
+  int nch;                      // selection chunks per unit = ceil(Nmax / kSelChunk)
+  int nbp;                      // histogram bins per chunk, padded (>= 128*G + 1)
+  unsigned long long* timeline; // [kTimelineSlots] %globaltimer stamps of the step (timing mode), or null
   int64_t wait_timeout_ns;
   int drop_flag_layer;
 };
 
 constexpr int kMaxLayers = 256;
+
+// timeline slots of the fused step kernel (ns of %globaltimer; first = first writer)
+enum Timeline : int {
+  TL_START = 0,          // first CTA started
+  TL_SEL_MISS_END = 1,   // last selection item of a missed unit finished
+  TL_SEL_PERS_END = 2,   // last selection item of a persistent unit finished
+  TL_FETCH_FIRST = 3,    // first fetch chunk could start copying
+  TL_FETCH_END = 4,      // last fetch chunk released
+  TL_ATT_FIRST = 5,      // first attention split started
+  TL_COMP_END = 6,       // last attention split finished
+  TL_FETCH_WAIT_NS = 7,  // summed waits of fetch warps on selections
+  TL_ATT_WAIT_NS = 8,    // summed waits of attention groups on fetch flags
+  kTimelineSlots = 16
+};
+constexpr int kSelChunk = 8192;  // tokens per selection chunk
+constexpr int kNBPad = 1056;     // >= 128 * kMaxG + 1, multiple of 32
 
 __host__ __device__ inline int64_t unit_of(const DevState& s, int l, int b, int h) {
   return ((int64_t)l * s.B + b) * s.Hkv + h;
@@ -140,6 +170,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -185,12 +221,12 @@ cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_
 cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st);
 cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st);
 cudaError_t launch_select(const DevState& s, int cluster, int64_t chunk, cudaStream_t st);
-cudaError_t launch_fetch_attend(const DevState& s, const uint16_t* q, float* out, cudaStream_t st);
+size_t select_smem_bytes(int G, int64_t chunk);
+cudaError_t launch_step_fused(const DevState& s, const uint16_t* q, float* out, cudaStream_t st);
 cudaError_t launch_resident_fill(const DevState& s, int64_t t0, int64_t t1, cudaStream_t st);
 cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
                               const uint16_t* vdev, cudaStream_t st);
 
-size_t select_smem_bytes(int G, int64_t chunk);
 
 }  // namespace clo
 

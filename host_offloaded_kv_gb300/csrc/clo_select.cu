@@ -1,4 +1,7 @@
-// Hash-code scoring and top-k selection of one unit per thread-block cluster.
+// Hash-code scoring and top-k selection of the units that missed, one unit per
+// thread-block cluster (runs before the fused step kernel, so the zero-copy fetch of
+// their rows can start at once; persistent units are selected inside the fused
+// kernel, under the fetch).
 //
 // score[t] = sum_g (128 - popcount(qcode_g ^ kcode_t)) over the G query heads of
 // the GQA group; the k = ceil(10 % of N) best tokens are kept, ties going to the
@@ -71,7 +74,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(DevState s, int64_t chun
   const int rank = (int)cluster.block_rank();
   const int64_t u = blockIdx.y;
   const int dec = s.decision[u];
-  if (dec == CLO_DEC_HIT) return;  // uniform over the cluster
+  if (dec != CLO_DEC_MISS) return;  // uniform over the cluster
 
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);

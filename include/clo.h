@@ -110,13 +110,14 @@ typedef struct clo_stats_t {
   int64_t timeouts;          /* ready-flag waits that gave up */
   int64_t last_hit, last_miss, last_persist, last_host_bytes, last_hbm_bytes_alg;
   int32_t warmup_done;       /* 1 once thresholds and persistent heads are fixed */
-  /* timing != 0: CUDA-event times of the phases (decide = reuse test and query
-   * hashing, select = scoring and top-k, fetch_attend = host-row fetch fused with
-   * sparse attention, total = whole step), for the last step and summed over the
+  /* timing != 0: CUDA-event times of the three launches of a step (decide = reuse
+   * test and query hashing; select = scoring and top-k of the missed units; fused =
+   * selection of the persistent units, host-row fetch and sparse attention in one
+   * persistent kernel) and of the whole step, for the last step and summed over the
    * timed_steps steps since the previous clo_stats call. */
   int32_t timed_steps;
-  float last_ms_decide, last_ms_select, last_ms_fetch_attend, last_ms_total;
-  double sum_ms_decide, sum_ms_select, sum_ms_fetch_attend, sum_ms_total;
+  float last_ms_decide, last_ms_select, last_ms_fused, last_ms_total;
+  double sum_ms_decide, sum_ms_select, sum_ms_fused, sum_ms_total;
 } clo_stats_t;
 
 /* Fill *cfg with defaults (shapes zero; topk_ratio 0.1; warmup_steps 16;
@@ -178,6 +179,13 @@ CLO_API const char* clo_last_error(void);
  *   CLO_DBG_PERSIST     uint8 [L][Hkv] persistent mask
  *   CLO_DBG_SHAT        fp64 [L][Hkv] warm-up mean similarity
  *   CLO_DBG_COS         fp32 [L][B][Hkv] cosines of the last step (NaN if none)
+ *   CLO_DBG_TIMELINE    uint64 [16] %globaltimer stamps (ns) of the last step's fused
+ *                       kernel, timing mode only (zeros otherwise): [0] start, [1] last
+ *                       selection of a missed unit done, [2] last selection of a
+ *                       persistent unit done, [3] first fetch chunk able to start,
+ *                       [4] last fetch chunk done, [5] first attention split, [6] last
+ *                       attention split done, [7] summed fetch waits on selections,
+ *                       [8] summed attention waits on fetch flags
  * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,
@@ -188,13 +196,15 @@ enum {
   CLO_DBG_TAU = 6,
   CLO_DBG_PERSIST = 7,
   CLO_DBG_SHAT = 8,
-  CLO_DBG_COS = 9
+  CLO_DBG_COS = 9,
+  CLO_DBG_TIMELINE = 10
 };
 CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int32_t seq, int32_t kvh, void* dst,
                                  int64_t dst_bytes);
 
-/* Change a debug setting after init (fault injection on the host side):
- * key CLO_SET_DROP_FLAG_LAYER (value: layer or -1), CLO_SET_WAIT_TIMEOUT_NS. */
+/* Change a setting after init:
+ *   CLO_SET_DROP_FLAG_LAYER  fault injection: layer whose fetch never signals, or -1
+ *   CLO_SET_WAIT_TIMEOUT_NS  bound of the device-side waits (> 0) */
 enum { CLO_SET_DROP_FLAG_LAYER = 1, CLO_SET_WAIT_TIMEOUT_NS = 2 };
 CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
 
