@@ -16,12 +16,8 @@ namespace clo {
 
 namespace {
 
-constexpr int kDecideThreads = 128;
-
-
-__device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, int64_t step, int warmup_active, int l,
-                            int b, int h, const uint16_t* Rs, float* qs, float (*red)[kDecideThreads / 32],
-                            int* s_dec_p, uint32_t (*words)[4]);
+constexpr int kDecideThreads = 512;  // one thread per (query head, code bit) for G <= 4
+constexpr int kDecideWarps = kDecideThreads / 32;
 
 struct StridedF32 {
   const float* p;
@@ -34,40 +30,43 @@ struct StridedBF16 {
   __device__ float operator()(int i) const { return bf16_bits_to_f32(p[i * stride]); }
 };
 
-// One CTA per unit; the head's projection R (d x 128 bf16) is staged in shared
-// memory with asynchronous 16-byte copies issued together, overlapping the
-// cosine of the reuse test.
+// One CTA per unit.  The head's projection R (d x 128 bf16) is staged in shared
+// memory by asynchronous 16-byte copies that overlap the reuse test; each thread
+// then hashes one (query head, code bit) pair.
 __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uint16_t* __restrict__ q, int64_t step,
                                                             int warmup_active) {
   __shared__ __align__(16) uint16_t Rs[kMaxD * 128];
   __shared__ float qs[kMaxG * kMaxD];
-  __shared__ float red[3][kDecideThreads / 32];
+  __shared__ float red[3][kDecideWarps];
   __shared__ int s_dec;
   __shared__ uint32_t words[kMaxG][4];
+  __shared__ unsigned char s_valid, s_persist;
+  __shared__ float s_tau;
+  __shared__ long long s_N, s_k;
 
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t u = blockIdx.x;
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
   const int l = (int)(u / ((int64_t)s.Hkv * s.B));
+  const int lh = l * s.Hkv + h;
+  const int G = s.G, d = s.d, GD = s.G * s.d;
   {
-    const uint4* src = reinterpret_cast<const uint4*>(s.R + ((int64_t)l * s.Hkv + h) * s.d * 128);
-    for (int e = threadIdx.x; e < s.d * 128 / 8; e += kDecideThreads) cp_async16(&Rs[e * 8], src + e);
+    const uint4* src = reinterpret_cast<const uint4*>(s.R + (int64_t)lh * d * 128);
+    for (int e = tid; e < d * 128 / 8; e += kDecideThreads) cp_async16(&Rs[e * 8], src + e);
     cp_async_commit();
   }
-  decide_unit(s, q, step, warmup_active, l, b, h, Rs, qs, red, &s_dec, words);
-}
+  // the unit's scalars, loaded in parallel by different warps
+  if (tid == 32) s_valid = s.qvalid[u];
+  if (tid == 64) s_persist = s.persist[lh];
+  if (tid == 96) s_tau = s.tau[lh];
+  if (tid == 128) s_N = s.ntok[b];
+  if (tid == 160) s_k = s.kcount[b];
 
-__device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, int64_t step, int warmup_active, int l,
-                            int b, int h, const uint16_t* Rs, float* qs, float (*red)[kDecideThreads / 32],
-                            int* s_dec_p, uint32_t (*words)[4]) {
-  int& s_dec = *s_dec_p;
-  const int64_t u = unit_of(s, l, b, h);
-  const int G = s.G, d = s.d, GD = s.G * s.d;
   const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * d;
   uint16_t* qc = s.qcache + u * GD;
-
   float dot = 0.f, nq = 0.f, nc = 0.f;
-  for (int e = threadIdx.x; e < GD; e += kDecideThreads) {
+  for (int e = tid; e < GD; e += kDecideThreads) {
     const float x = bf16_bits_to_f32(qg[e]);
     const float c = bf16_bits_to_f32(qc[e]);
     qs[e] = x;
@@ -78,48 +77,46 @@ __device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, i
   dot = warp_sum(dot);
   nq = warp_sum(nq);
   nc = warp_sum(nc);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     red[0][warp] = dot;
     red[1][warp] = nq;
     red[2][warp] = nc;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     float D = 0.f, Q = 0.f, C = 0.f;
-    for (int w = 0; w < kDecideThreads / 32; ++w) {
+    for (int w = 0; w < kDecideWarps; ++w) {
       D += red[0][w];
       Q += red[1][w];
       C += red[2][w];
     }
-    const bool valid = s.qvalid[u] != 0;
-    float cosv = (Q > 0.f && C > 0.f) ? D / (sqrtf(Q) * sqrtf(C)) : 0.f;
-    const int lh = l * s.Hkv + h;
+    const bool valid = s_valid != 0;
+    const float cosv = (Q > 0.f && C > 0.f) ? D / (sqrtf(Q) * sqrtf(C)) : 0.f;
     int dec;
     if (warmup_active) {
       dec = CLO_DEC_MISS;
       if (step >= 1 && valid) atomicAdd(&s.shat_sum[lh], (double)cosv);
-    } else if (s.persist[lh]) {
+    } else if (s_persist) {
       dec = CLO_DEC_PERSIST;
     } else if (!valid) {
       dec = CLO_DEC_MISS;
     } else {
-      dec = (cosv >= s.tau[lh]) ? CLO_DEC_HIT : CLO_DEC_MISS;
+      dec = (cosv >= s_tau) ? CLO_DEC_HIT : CLO_DEC_MISS;
     }
     s.decision[u] = (uint8_t)dec;
     s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
     s_dec = dec;
-    // per-layer work lists of the fused step kernel: hit, persistent, missed
+  }
+  __syncthreads();
+  const int dec = s_dec;
+  if (tid == 32) {  // bookkeeping off the critical path: work lists and counters
+    const bool valid = s_valid != 0;
     const int BH = s.B * s.Hkv;
     const int li = dec == CLO_DEC_HIT ? 0 : (dec == CLO_DEC_PERSIST ? 1 : 2);
     int32_t* lst = li == 0 ? s.hit_list : (li == 1 ? s.pers_list : s.miss_list);
     lst[(int64_t)l * BH + atomicAdd(&s.lcnt[li * s.L + l], 1)] = (int32_t)u;
-
-    // counters: decisions, host bytes, algorithmic HBM bytes of this unit's step
-    const int64_t N = s.ntok[b];
-    const int64_t k = s.kcount[b];
-    const int64_t rec = 4LL * d;
-    unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
+    const int64_t N = s_N, k = s_k, rec = 4LL * d;
+    const unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
     int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
     if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
     if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
@@ -134,51 +131,38 @@ __device__ void decide_unit(const DevState& s, const uint16_t* __restrict__ q, i
     atomicAdd(&s.step_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
     atomicAdd(&s.total_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
   }
-  __syncthreads();
-  const int dec = s_dec;
   if (dec == CLO_DEC_MISS) {
-    for (int e = threadIdx.x; e < GD; e += kDecideThreads) qc[e] = qg[e];
-    if (threadIdx.x == 0) s.qvalid[u] = 1;
+    for (int e = tid; e < GD; e += kDecideThreads) qc[e] = qg[e];
+    if (tid == 0) s.qvalid[u] = 1;
   }
   cp_async_wait<0>();  // R staged (also before any exit: no copy may outlive the CTA)
   __syncthreads();
   if (dec == CLO_DEC_HIT) return;  // uniform over the CTA
 
-  // query codes of the G heads: thread j computes bit j of every head
-  const int j = threadIdx.x;  // 128 threads = 128 bits
-  const uint16_t* Rg = Rs;
-  float acc[kMaxG], aab[kMaxG];
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) acc[g] = aab[g] = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < d; ++i) {
-    const float r = bf16_bits_to_f32(Rg[i * 128 + j]);
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      if (g < G) {
-        const float x = qs[g * d + i];
-        acc[g] = fmaf(x, r, acc[g]);
-        aab[g] = fmaf(fabsf(x), fabsf(r), aab[g]);
-      }
+  // query codes: thread (g, j) computes bit j of head g
+  const int j = tid & 127;
+  for (int g = tid >> 7; g < G; g += kDecideThreads / 128) {
+    const float* xg = qs + g * d;
+    float acc = 0.f, aab = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < d; ++i) {
+      const float x = xg[i];
+      const float r = bf16_bits_to_f32(Rs[i * 128 + j]);
+      acc = fmaf(x, r, acc);
+      aab = fmaf(fabsf(x), fabsf(r), aab);
     }
-  }
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) {
-    if (g < G) {
-      bool bit;
-      if (sign_certified_f32(acc[g], aab[g], d))
-        bit = acc[g] > 0.f;
-      else
-        bit = hash_bit_slow(StridedF32{qs + g * d, 1}, StridedBF16{Rg + j, 128}, d);
-      const uint32_t w = __ballot_sync(0xffffffffu, bit);
-      if (lane == 0) words[g][warp] = w;
-    }
+    bool bit;
+    if (sign_certified_f32(acc, aab, d))
+      bit = acc > 0.f;
+    else
+      bit = hash_bit_slow(StridedF32{xg, 1}, StridedBF16{Rs + j, 128}, d);
+    const uint32_t w = __ballot_sync(0xffffffffu, bit);
+    if (lane == 0) words[g][(tid & 127) >> 5] = w;
   }
   __syncthreads();
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    s.qcodes[((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G + g] =
-        make_uint4(words[g][0], words[g][1], words[g][2], words[g][3]);
+  if (tid < G) {
+    s.qcodes[((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G + tid] =
+        make_uint4(words[tid][0], words[tid][1], words[tid][2], words[tid][3]);
   }
 }
 
