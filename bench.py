@@ -280,7 +280,7 @@ def run_gb300(args, rank, world, local_rank):
     hits = st["units_hit"] - before["units_hit"]
     miss = st["units_miss"] - before["units_miss"]
     pers = st["units_persist"] - before["units_persist"]
-    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "select", "fused")}
+    phases = {p: st[f"sum_ms_{p}"] for p in ("decide", "fused")}
     ms_total = max_over_ranks(ms_total, world)
     del qdev
 
@@ -325,12 +325,9 @@ def run_gb300(args, rank, world, local_rank):
     fu_s = phases["fused"] / 1e3
     kern["fused"].update(
         bound="host-link", achieved_gbs=fetch_bytes / fu_s / 1e9 if fetch_bytes else 0.0, peak_gbs=link_gbs,
-        hbm_gbs=(attend_hbm + fetch_bytes + pers * (N * 16 + kmax * 4)) / fu_s / 1e9,
-        note="host bytes over the link / kernel time; hbm_gbs = (code reads of the persistent units' selections "
+        hbm_gbs=(attend_hbm + fetch_bytes + select_hbm) / fu_s / 1e9,
+        note="host bytes over the link / kernel time; hbm_gbs = (code reads and index writes of the selections "
              "+ attention row reads + slot writes) / kernel time")
-    sel_s = phases["select"] / 1e3
-    kern["select"].update(bound="hbm", achieved_gbs=miss * (N * 16 + kmax * 4) / sel_s / 1e9 if sel_s else None,
-                          peak_gbs=hbm_peak, note="code reads + index writes of the missed units' selections")
     dom = "fused"
     dk = kern[dom]
     traffic = traffic_from_profiles(dom, w.name)

@@ -62,8 +62,8 @@ class clo_stats_t(ctypes.Structure):
         "steps", "units_hit", "units_miss", "units_persist", "host_bytes", "hbm_bytes_alg", "timeouts",
         "last_hit", "last_miss", "last_persist", "last_host_bytes", "last_hbm_bytes_alg")] + \
         [("warmup_done", ctypes.c_int32), ("timed_steps", ctypes.c_int32)] + \
-        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_select", "last_ms_fused", "last_ms_total")] + \
-        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_select", "sum_ms_fused", "sum_ms_total")]
+        [(n, ctypes.c_float) for n in ("last_ms_decide", "last_ms_fused", "last_ms_total")] + \
+        [(n, ctypes.c_double) for n in ("sum_ms_decide", "sum_ms_fused", "sum_ms_total")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -300,4 +300,8 @@ class CLOContext:
         return {"sel_missed_done_us": rel(t[1]), "sel_persistent_done_us": rel(t[2]),
                 "first_fetch_us": rel(t[3]), "fetch_done_us": rel(t[4]), "first_attention_us": rel(t[5]),
                 "attention_done_us": rel(t[6]), "fetch_wait_sum_us": round(int(t[7]) / 1e3, 1),
-                "attention_wait_sum_us": round(int(t[8]) / 1e3, 1)}
+                "attention_wait_sum_us": round(int(t[8]) / 1e3, 1),
+                "selection_chunk_mean_us": round(int(t[9]) / 1e3 / max(1, int(t[10])), 2),
+                "selection_chunks": int(t[10]),
+                "attention_split_mean_us": round(int(t[11]) / 1e3 / max(1, int(t[12])), 2),
+                "attention_splits": int(t[12])}

@@ -35,9 +35,7 @@ clo_status fail(clo_status st, const std::string& msg) {
     if (e_ != cudaSuccess) return fail(CLO_ERR_CUDA, std::string(#expr) + ": " + cudaGetErrorString(e_)); \
   } while (0)
 
-constexpr int kSplitRows = 256;
 constexpr int64_t kStageTokens = 16384;
-constexpr int64_t kSelClusterChunk = 16384;
 
 int64_t topk_for(int64_t N, int64_t topk, double ratio) {
   if (N <= 0) return 0;
@@ -63,14 +61,12 @@ struct clo_ctx {
   bool warmup_mode = false;
   int W = 0;
   bool warmup_done = false;
-  int sel_cluster = 1;
-  int64_t sel_chunk = 0;
   uint16_t* kstage = nullptr;
   uint16_t* vstage = nullptr;
   uint16_t* q_io = nullptr;
   float* out_io = nullptr;
   // per-step phase events (timing mode): 4 markers per step, reused after clo_stats
-  std::vector<std::array<cudaEvent_t, 4>> ev_pool;
+  std::vector<std::array<cudaEvent_t, 3>> ev_pool;
   size_t ev_used = 0;
   uint32_t epoch = 0;
   uint32_t* step_zero = nullptr;  // zeroed at the start of every step
@@ -201,8 +197,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   s.pool = static_cast<const uint16_t*>(pd);
   s.wait_timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : 2000000000LL;
   s.drop_flag_layer = cfg->debug_drop_flag_layer;
-  s.split_rows = kSplitRows;
   s.nsplit = (int)((c->kmax + kSplitRows - 1) / kSplitRows);
+  s.nchunk = (int)((c->kmax + kChunkRows - 1) / kChunkRows);
   const int64_t U = c->U;
   const int LH = c->L * c->Hkv;
   int64_t* ntok_d = nullptr;
@@ -244,9 +240,11 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     const size_t o_queue = off;
     off += 4;
     const size_t o_ready = off;
-    off += (size_t)U * s.nsplit;
+    off += (size_t)U * s.nchunk;
     const size_t o_sel = off;
-    off += 3 * (size_t)U;
+    off += 4 * (size_t)U;
+    const size_t o_hist = off;
+    off += (size_t)U * s.nbp;
     off = (off + 1) / 2 * 2;  // 8-byte alignment for the timeline
     const size_t o_tl = off;
     off += 2 * (size_t)kTimelineSlots;
@@ -260,19 +258,21 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.ready = z + o_ready;
     s.score_done = z + o_sel;
     s.fin_done = z + o_sel + U;
-    s.sel_cnt = z + o_sel + 2 * U;
+    s.cnt_done = z + o_sel + 2 * U;
+    s.sel_cnt = z + o_sel + 3 * U;
+    s.unit_hist = z + o_hist;
     c->timeline_dev = reinterpret_cast<unsigned long long*>(z + o_tl);
     s.timeline = cfg->timing ? c->timeline_dev : nullptr;
   }
   CLO_TRY(c->dalloc(&s.hit_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.pers_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.miss_list, (size_t)c->L * c->B * c->Hkv));
-  CLO_TRY(c->dalloc(&s.sel_hist, (size_t)U * s.nch * s.nbp));
   CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * s.nch));
+  CLO_TRY(c->dalloc(&s.sel_thr, (size_t)U));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
   CLO_TRY(c->dalloc(&s.err, 1));
   CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));
-  CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * c->G * (c->d + 2)));
+  CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * kPartsPerSplit * c->G * (c->d + 2)));
 
   std::vector<int32_t> pslot((size_t)LH, -1);
   std::vector<uint8_t> pm((size_t)LH, 0);
@@ -372,7 +372,6 @@ CLO_API clo_status clo_append_kv(clo_ctx* c, int32_t layer, int32_t seq, const v
 }
 
 static clo_status refresh_lengths(clo_ctx* c) {
-  int64_t nmax = 0;
   for (int b = 0; b < c->B; ++b) {
     const int64_t n0 = c->ntok[b];
     for (int l = 1; l < c->L; ++l)
@@ -380,7 +379,6 @@ static clo_status refresh_lengths(clo_ctx* c) {
         return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has layers of different lengths");
     if (n0 < 1) return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has no K/V appended");
     c->ntok_pinned[b] = n0;
-    nmax = std::max(nmax, n0);
   }
   int32_t* kc = reinterpret_cast<int32_t*>(c->ntok_pinned + c->B);
   for (int b = 0; b < c->B; ++b) kc[b] = (int32_t)topk_for(c->ntok[b], c->cfg.topk, c->cfg.topk_ratio);
@@ -389,13 +387,6 @@ static clo_status refresh_lengths(clo_ctx* c) {
   CLO_CUDA(cudaMemcpyAsync(const_cast<int32_t*>(c->ds.kcount), kc, sizeof(int32_t) * c->B, cudaMemcpyHostToDevice,
                            c->stream));
   CLO_CUDA(cudaStreamSynchronize(c->stream));  // the pinned staging is reused
-  // selection of missed units: a cluster of CTAs per unit, chunks of <= 16K tokens
-  int C = 1;
-  while (C < 8 && (nmax + C - 1) / C > kSelClusterChunk) C *= 2;
-  int64_t chunk = (nmax + C - 1) / C;
-  chunk = (chunk + 511) / 512 * 512;
-  c->sel_cluster = C;
-  c->sel_chunk = chunk;
   c->ntok_dirty = false;
   return CLO_OK;
 }
@@ -422,7 +413,7 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   cudaEvent_t* ev = nullptr;
   if (timed) {
     if (c->ev_used == c->ev_pool.size()) {
-      std::array<cudaEvent_t, 4> set{};
+      std::array<cudaEvent_t, 3> set{};
       for (auto& e : set) CLO_CUDA(cudaEventCreate(&e));
       c->ev_pool.push_back(set);
     }
@@ -433,10 +424,8 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
   CLO_CUDA(cudaMemsetAsync(c->step_zero, 0, c->step_zero_bytes, c->stream));
   CLO_CUDA(launch_decide(s, qd, c->step, warm ? 1 : 0, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[1], c->stream));
-  CLO_CUDA(launch_select(s, c->sel_cluster, c->sel_chunk, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
   CLO_CUDA(launch_step_fused(s, qd, od, c->stream));
-  if (timed) CLO_CUDA(cudaEventRecord(ev[3], c->stream));
+  if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
   if (warm && c->step == c->W - 1) {
     CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
     CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
@@ -478,20 +467,17 @@ CLO_API clo_status clo_stats(clo_ctx* c, clo_stats_t* out) {
   out->timed_steps = (int32_t)c->ev_used;
   for (size_t i = 0; i < c->ev_used; ++i) {
     const cudaEvent_t* e = c->ev_pool[i].data();
-    float t[4];
+    float t[3];
     CLO_CUDA(cudaEventElapsedTime(&t[0], e[0], e[1]));
     CLO_CUDA(cudaEventElapsedTime(&t[1], e[1], e[2]));
-    CLO_CUDA(cudaEventElapsedTime(&t[2], e[2], e[3]));
-    CLO_CUDA(cudaEventElapsedTime(&t[3], e[0], e[3]));
+    CLO_CUDA(cudaEventElapsedTime(&t[2], e[0], e[2]));
     out->sum_ms_decide += t[0];
-    out->sum_ms_select += t[1];
-    out->sum_ms_fused += t[2];
-    out->sum_ms_total += t[3];
+    out->sum_ms_fused += t[1];
+    out->sum_ms_total += t[2];
     if (i + 1 == c->ev_used) {
       out->last_ms_decide = t[0];
-      out->last_ms_select = t[1];
-      out->last_ms_fused = t[2];
-      out->last_ms_total = t[3];
+      out->last_ms_fused = t[1];
+      out->last_ms_total = t[2];
     }
   }
   c->ev_used = 0;

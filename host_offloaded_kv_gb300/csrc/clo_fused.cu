@@ -3,7 +3,7 @@
 // attention, ordered by device-side flags only.  (Missed units are selected by the
 // launch just before, so their fetch can start as soon as this kernel does.)
 //
-// Each CTA holds one fetch warp and one 4-warp compute group (6 CTAs per SM).  One
+// Each CTA holds one fetch warp and one 4-warp compute group (3 CTAs per SM).  One
 // fetch warp per CTA keeps enough host-link requests in flight to saturate the link
 // without queueing so many that the HBM traffic of the compute groups waits behind
 // them.
@@ -29,39 +29,21 @@
 // Every wait targets work that sits earlier in the compute queue (or a fetch, which
 // itself waits only on earlier compute items), so the waits form no cycle; each
 // wait is bounded by the context's timeout and reports CLO_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+#include <stdlib.h>
+
 #include "clo_internal.cuh"
 
 namespace clo {
 
 namespace {
 
-constexpr int kFetchWarps = 1;
 constexpr int kCompWarps = 4;
 constexpr int kCompThreads = 32 * kCompWarps;
-constexpr int kFThreads = 32 * (kFetchWarps + kCompWarps);
-constexpr int kFetchUnroll = 8;
-constexpr int kAttTile = 32;
-constexpr int kSelTile = 512;  // tokens per bulk copy (8 KB)
-constexpr int kSelStages = 3;
-constexpr int kMaxChunks = (int)(kMaxTokens / kSelChunk);
-constexpr uint64_t kMbarLimitNs = 2000000000ull;
+constexpr int kFetchUnroll = 4;
+static_assert(kCompWarps == kPartsPerSplit, "one attention partial per compute warp");
 
 __device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
-
-// Barrier of the compute group that also ANDs a predicate over its threads, so a
-// decision taken per thread (a bounded wait that may time out) becomes uniform.
-__device__ __forceinline__ bool comp_bar_and(bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred a, b;\n\t"
-      "setp.ne.u32 a, %1, 0;\n\t"
-      "bar.red.and.pred b, 1, %2, a;\n\t"
-      "selp.u32 %0, 1, 0, b;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)p), "n"(kCompThreads)
-      : "memory");
-  return r != 0;
-}
 
 __device__ __forceinline__ int layer_of(const int* pre, int L, int p) {
   int lo = 0, hi = L;
@@ -92,69 +74,27 @@ __device__ void wait_flag(const uint32_t* flag, uint32_t target, const DevState&
   }
 }
 
-template <int D>
+template <int D, int NBUF>
 struct AttSmem {
-  static constexpr int ROWW = 2 * D + 8;  // bf16 per smem row, padded by 16 bytes
-  static constexpr int NG = kCompThreads / D;
-  float qs[kMaxG][D];
-  uint16_t rows[kAttTile][ROWW];
-  float sc[kMaxG][kAttTile];
-  float m_run[kMaxG], l_run[kMaxG], alpha[kMaxG];
-  float red[NG > 1 ? NG : 1][kMaxG][D];
+  static constexpr int ROWW = 2 * D + 8;     // bf16 per smem row (K | V), padded by 16 bytes
+  uint16_t rows[kCompWarps][NBUF][16][ROWW];  // 16-row chunks per warp (NBUF = 2: double buffer)
+  float red[kCompWarps];
   int last;
 };
 
 struct SelSmem {
-  uint4 ring[kSelStages][kSelTile];
-  uint32_t hist[kNBPad];
-  int cgt[kMaxChunks], ceq[kMaxChunks];
+  uint16_t scores[kSelChunk];  // scores of the chunk's tokens
+  uint32_t hist[kNBPad];       // histogram of the chunk's scores
+  uint32_t tot[kNBPad];        // the unit's histogram (last chunk to arrive)
   int wc[kCompWarps][2];
-  int misc[4];
+  int misc[8];
 };
 
-template <int D>
+template <int D, int NBUF>
 union CompSmem {
-  AttSmem<D> att;
+  AttSmem<D, NBUF> att;
   SelSmem sel;
 };
-
-struct Ring {
-  uint64_t* bar;
-  uint32_t n;  // tiles consumed so far by this group (uniform over the group)
-};
-
-// Streams tiles of a unit's chunk of codes through the ring; calls f(tile_index, tile_ptr, ntok).
-template <class F>
-__device__ void stream_codes(const DevState& s, SelSmem& sm, Ring& ring, const uint4* src, int len, int gtid, F f) {
-  const int ntiles = (len + kSelTile - 1) / kSelTile;
-  const uint32_t n0 = ring.n;
-  // the ring shares shared memory with the attention buffers written by generic stores
-  fence_proxy_async_smem();
-  comp_bar();
-  if (gtid == 0) {
-    for (int i = 0; i < kSelStages && i < ntiles; ++i) {
-      const int st = (int)((n0 + i) % kSelStages);
-      const int n = (len - i * kSelTile) < kSelTile ? (len - i * kSelTile) : kSelTile;
-      mbar_arrive_expect_tx(&ring.bar[st], (uint32_t)n * 16u);
-      bulk_copy_g2s(&sm.ring[st][0], src + (int64_t)i * kSelTile, (uint32_t)n * 16u, &ring.bar[st]);
-    }
-  }
-  for (int i = 0; i < ntiles; ++i) {
-    const uint32_t tn = n0 + i;
-    const int st = (int)(tn % kSelStages);
-    const int n = (len - i * kSelTile) < kSelTile ? (len - i * kSelTile) : kSelTile;
-    const bool ok = comp_bar_and(mbar_wait_bounded(&ring.bar[st], (tn / kSelStages) & 1u, s.err, kMbarLimitNs));
-    if (ok) f(i, &sm.ring[st][0], n);  // uniform: f may use group barriers
-    comp_bar();
-    if (gtid == 0 && i + kSelStages < ntiles) {
-      const int j = i + kSelStages;
-      const int nj = (len - j * kSelTile) < kSelTile ? (len - j * kSelTile) : kSelTile;
-      mbar_arrive_expect_tx(&ring.bar[st], (uint32_t)nj * 16u);
-      bulk_copy_g2s(&sm.ring[st][0], src + (int64_t)j * kSelTile, (uint32_t)nj * 16u, &ring.bar[st]);
-    }
-  }
-  ring.n = n0 + ntiles;
-}
 
 template <int G>
 __device__ __forceinline__ int score_of(const uint4 c, const uint64_t* qw) {
@@ -180,178 +120,269 @@ __device__ __forceinline__ void load_qcodes(const DevState& s, int64_t u, uint64
   }
 }
 
-// ---- selection items ----------------------------------------------------------------
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// ---- selection item: one chunk of kSelChunk tokens of one unit --------------------------
+// Scores are small integers (0 .. 128 G), so the top-k is one histogram digit:
+//   1. score the chunk's tokens (16-byte codes read once, coalesced), keep the scores in
+//      shared memory, build the chunk's histogram and add it into the unit's histogram;
+//   2. the chunk that arrives last finds the unit's threshold T, the largest score with
+//      count(score >= T) >= k, and publishes T and n_gt = count(score > T);
+//   3. each chunk publishes its counts above and at T; from the counts of the chunks
+//      before it, a chunk knows where its indices go and how many of its ties it takes
+//      (ties go to the lowest token index: the quota k - n_gt is filled in chunk order);
+//   4. ordered compaction of the chunk from the scores in shared memory.
+// The chunks of a unit sit next to each other in the work queue and every group runs its
+// item to the end, so the waits of steps 2 and 3 only target items already running
+// (provided at least nch groups run; the host checks this).
 template <int G>
-__device__ void sel_score(const DevState& s, SelSmem& sm, Ring& ring, int64_t u, int c, int gtid) {
+__device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int gtid) {
+  constexpr int NB = 128 * G + 1;
+  constexpr int kU = 8;  // code loads in flight per thread
+  const int NC = s.nch;
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
+  const int k = s.kcount[b];
   const int64_t t0 = (int64_t)c * kSelChunk;
   const int len = (int)(N - t0 <= 0 ? 0 : (N - t0 < kSelChunk ? N - t0 : kSelChunk));
-  for (int i = gtid; i < s.nbp; i += kCompThreads) sm.hist[i] = 0;
+  const int warp = gtid >> 5, lane = gtid & 31;
+  for (int i = gtid; i < NB; i += kCompThreads) sm.hist[i] = 0;
   uint64_t qw[2 * G];
   load_qcodes<G>(s, u, qw);
   comp_bar();
-  stream_codes(s, sm, ring, s.codes + u * s.Nmax + t0, len, gtid, [&](int, const uint4* tile, int n) {
-    for (int t = gtid; t < n; t += kCompThreads) atomicAdd(&sm.hist[score_of<G>(tile[t], qw)], 1u);
-  });
-  uint32_t* H = s.sel_hist + (u * s.nch + c) * s.nbp;
-  for (int i = gtid; i < s.nbp; i += kCompThreads) H[i] = sm.hist[i];
-  __threadfence();
-  comp_bar();
-  if (gtid == 0) red_release_add_u32(&s.score_done[u], 1u);
-}
 
-template <int G>
-__device__ void sel_finalize(const DevState& s, SelSmem& sm, int64_t u, int gtid) {
-  constexpr int NB = 128 * G + 1;
-  const int b = (int)((u / s.Hkv) % s.B);
-  const int64_t k = s.kcount[b];
-  const int nch = s.nch;
-  if (gtid == 0) wait_flag(&s.score_done[u], (uint32_t)nch, s);
-  if (gtid < 4) sm.misc[gtid] = 0;
-  comp_bar();
-  const uint32_t* H = s.sel_hist + u * nch * s.nbp;
-  for (int bin = gtid; bin < NB; bin += kCompThreads) {
-    uint32_t t = 0;
-    for (int c = 0; c < nch; ++c) t += __ldcg(H + c * s.nbp + bin);
-    sm.hist[bin] = t;
-  }
-  comp_bar();
-  if (gtid < 32) {  // threshold: largest T with count(score >= T) >= k
-    const int lane = gtid;
-    const int seg = (NB + 31) / 32;
-    const int hi = NB - lane * seg;
-    const int lo = hi - seg > 0 ? hi - seg : 0;
-    int segsum = 0;
-    for (int bin = lo; bin < hi; ++bin) segsum += (int)sm.hist[bin];
-    int incl = segsum;
+  // 1. scores and histograms
+  const uint4* src = s.codes + u * s.Nmax + t0;
+  for (int base = 0; base < len; base += kCompThreads * kU) {
+    uint4 cv[kU];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+    for (int j = 0; j < kU; ++j) {
+      const int t = base + kCompThreads * j + gtid;
+      if (t < len) cv[j] = ld_nc_v4(src + t);
     }
-    const int excl = incl - segsum;
-    if (excl < k && incl >= k) {
-      int run = excl;
-      for (int bin = hi - 1; bin >= lo; --bin) {
-        if (run + (int)sm.hist[bin] >= k) {
-          sm.misc[0] = bin;
-          sm.misc[1] = run;
-          break;
-        }
-        run += (int)sm.hist[bin];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int t = base + kCompThreads * j + gtid;
+      if (t < len) {
+        const int sc = score_of<G>(cv[j], qw);
+        sm.scores[t] = (uint16_t)sc;
+        atomicAdd(&sm.hist[sc], 1u);
       }
     }
   }
   comp_bar();
-  const int T = sm.misc[0], n_gt = sm.misc[1];
-  for (int c = gtid; c < nch; c += kCompThreads) {
-    int gt = 0;
-    for (int bin = T + 1; bin < NB; ++bin) gt += (int)__ldcg(H + c * s.nbp + bin);
-    sm.cgt[c] = gt;
-    sm.ceq[c] = (int)__ldcg(H + c * s.nbp + T);
-  }
-  comp_bar();
-  if (gtid == 0) {
-    const int quota = (int)k - n_gt;
-    int off = 0, eqb = 0;
-    for (int c = 0; c < nch; ++c) {
-      int take = quota - eqb;
-      take = take < 0 ? 0 : (take > sm.ceq[c] ? sm.ceq[c] : take);
-      s.sel_meta[u * nch + c] = make_int4(off, take, T, 0);
-      off += sm.cgt[c] + take;
-      eqb += sm.ceq[c];
-    }
+  uint32_t* UH = s.unit_hist + u * s.nbp;
+  for (int i = gtid; i < NB; i += kCompThreads) {
+    const uint32_t v = sm.hist[i];
+    if (v) atomicAdd(UH + i, v);
   }
   __threadfence();
   comp_bar();
-  if (gtid == 0) red_release_add_u32(&s.fin_done[u], 1u);
-}
-
-template <int G>
-__device__ void sel_compact(const DevState& s, SelSmem& sm, Ring& ring, int64_t u, int c, int gtid) {
-  const int b = (int)((u / s.Hkv) % s.B);
-  const int64_t N = s.ntok[b];
-  const int64_t k = s.kcount[b];
-  const int64_t t0 = (int64_t)c * kSelChunk;
-  const int len = (int)(N - t0 <= 0 ? 0 : (N - t0 < kSelChunk ? N - t0 : kSelChunk));
-  if (gtid == 0) wait_flag(&s.fin_done[u], 1u, s);
-  uint64_t qw[2 * G];
-  load_qcodes<G>(s, u, qw);
+  if (gtid == 0) sm.misc[0] = atom_add_acq_rel(&s.score_done[u], 1u) == (uint32_t)NC - 1u;
   comp_bar();
-  const int4 meta = __ldcg(&s.sel_meta[u * s.nch + c]);
-  const int off = meta.x, take = meta.y, T = meta.z;
-  const int warp = gtid >> 5, lane = gtid & 31;
-  const uint32_t lt = (1u << lane) - 1u;
-  int32_t* out = s.idx + u * s.kmax;
-  int run_eq = 0, run_sel = 0;  // chunk-local, uniform over the group
-  stream_codes(s, sm, ring, s.codes + u * s.Nmax + t0, len, gtid, [&](int ti, const uint4* tile, int n) {
-    int sc[4];
-    int gt = 0, eq = 0;
+
+  // 2. threshold (last chunk to arrive) or wait for it
+  if (sm.misc[0]) {
+    for (int i = gtid; i < NB; i += kCompThreads) sm.tot[i] = __ldcg(UH + i);
+    comp_bar();
+    if (warp == 0) {
+      const int seg = (NB + 31) / 32;
+      const int hi = NB - lane * seg;
+      const int lo = hi - seg > 0 ? hi - seg : 0;
+      int segsum = 0;
+      for (int bin = lo; bin < hi; ++bin) segsum += (int)sm.tot[bin];
+      int incl = segsum;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = 128 * warp + 32 * i + lane;
-      sc[i] = t < n ? score_of<G>(tile[t], qw) : -1;
-      gt += __popc(__ballot_sync(0xffffffffu, sc[i] > T));
-      eq += __popc(__ballot_sync(0xffffffffu, sc[i] == T));
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - segsum;
+      if (excl < k && incl >= k) {
+        int run = excl;
+        for (int bin = hi - 1; bin >= lo; --bin) {
+          if (run + (int)sm.tot[bin] >= k) {
+            s.sel_thr[u] = make_int2(bin, run);
+            break;
+          }
+          run += (int)sm.tot[bin];
+        }
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_add_u32(&s.fin_done[u], 1u);
+    }
+  }
+  if (gtid == 0) {
+    wait_flag(&s.fin_done[u], 1u, s);
+    const int2 th = __ldcg(&s.sel_thr[u]);
+    sm.misc[1] = th.x < 0 ? 0 : (th.x >= NB ? NB - 1 : th.x);  // clamped: garbage only after a timeout
+    sm.misc[2] = th.y;
+  }
+  comp_bar();
+  const int T = sm.misc[1], n_gt = sm.misc[2];
+  const int quota = k - n_gt;  // ties to take, unit-wide, lowest index first
+
+  // 3. this chunk's counts; offsets from the chunks before it
+  if (warp == 0) {
+    int gt = 0;
+    for (int bin = T + 1 + lane; bin < NB; bin += 32) gt += (int)sm.hist[bin];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    if (lane == 0) {
+      s.sel_meta[u * NC + c] = make_int2(gt, (int)sm.hist[T]);
+      __threadfence();
+      red_release_add_u32(&s.cnt_done[u], 1u);
+      wait_flag(&s.cnt_done[u], (uint32_t)NC, s);
+    }
+    __syncwarp();
+    int base_sel = 0, eq_before = 0;
+    for (int c0 = 0; c0 < c; c0 += 32) {
+      const int2 m = (c0 + lane < c) ? __ldcg(&s.sel_meta[u * NC + c0 + lane]) : make_int2(0, 0);
+      int ie = m.y;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, ie, o);
+        if (lane >= o) ie += v;
+      }
+      int take = quota - (eq_before + ie - m.y);
+      take = take < 0 ? 0 : (take > m.y ? m.y : take);
+      int sel = m.x + take;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
+      base_sel += sel;
+      eq_before += __shfl_sync(0xffffffffu, ie, 31);
+    }
+    if (lane == 0) {
+      sm.misc[3] = base_sel;
+      sm.misc[4] = eq_before;
+    }
+  }
+  comp_bar();
+  const int out_base = sm.misc[3];
+  int take_eq = quota - sm.misc[4];
+  take_eq = take_eq < 0 ? 0 : (take_eq > (int)sm.hist[T] ? (int)sm.hist[T] : take_eq);
+
+  // 4. ordered compaction: warp w owns tokens [w * seg, (w + 1) * seg) of the chunk
+  const int wseg = ((len + kCompWarps - 1) / kCompWarps + 31) / 32 * 32;
+  const int w0 = warp * wseg;
+  const int w1 = (w0 + wseg < len) ? w0 + wseg : len;
+  {
+    int gt = 0, eq = 0;
+    for (int t = w0 + lane; t < w1; t += 32) {
+      const int sc = sm.scores[t];
+      gt += sc > T;
+      eq += sc == T;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
     }
     if (lane == 0) {
       sm.wc[warp][0] = gt;
       sm.wc[warp][1] = eq;
     }
-    comp_bar();
-    int eqb = run_eq, selb = run_sel, eq_all = 0, sel_all = 0;
-    for (int w = 0; w < kCompWarps; ++w) {
-      int tk = take - (run_eq + eq_all);
-      tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);
-      const int selw = sm.wc[w][0] + tk;
-      if (w < warp) {
-        eqb += sm.wc[w][1];
-        selb += selw;
-      }
-      eq_all += sm.wc[w][1];
-      sel_all += selw;
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool is_eq = sc[i] == T;
+  }
+  comp_bar();
+  int off = out_base, eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    int tk = take_eq - eqb;
+    tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);
+    off += sm.wc[w][0] + tk;
+    eqb += sm.wc[w][1];
+  }
+  {
+    const uint32_t lt = (1u << lane) - 1u;
+    int32_t* out = s.idx + u * s.kmax;
+    for (int base = w0; base < w1; base += 32) {
+      const int t = base + lane;
+      const int sc = t < w1 ? (int)sm.scores[t] : -1;
+      const bool is_eq = sc == T;
       const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-      const int rank = eqb + __popc(beq & lt);
-      const bool sel = sc[i] > T || (is_eq && rank < take);
+      const bool sel = sc > T || (is_eq && eqb + __popc(beq & lt) < take_eq);
       const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
       if (sel) {
-        const int pos = off + selb + __popc(bsel & lt);
+        const int pos = off + __popc(bsel & lt);
         if (pos < k)
-          out[pos] = (int32_t)(t0 + (int64_t)ti * kSelTile + 128 * warp + 32 * i + lane);
+          out[pos] = (int32_t)(t0 + t);
         else
           atomicOr(s.err, kErrBounds);
       }
       eqb += __popc(beq);
-      selb += __popc(bsel);
+      off += __popc(bsel);
     }
-    run_eq += eq_all;
-    run_sel += sel_all;
-  });
+  }
   __threadfence();
   comp_bar();
   if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
 }
 
 // ---- attention split -----------------------------------------------------------------
-template <int D>
-__device__ void attend_split(const DevState& s, AttSmem<D>& sm, const uint16_t* __restrict__ q,
+// Tensor-core (mma.sync m16n8k16, bf16 in, fp32 accumulate) split attention.  A split
+// is kSplitRows = 1024 selected rows; each of the 4 warps takes 256 of them in
+// double-buffered chunks of 16 (the next chunk's copy overlaps this chunk's math):
+//   S[16 rows x 8 heads] = K[16 x d] . Q^T[d x 8]      (G <= 8 query heads of the group
+//                                                         on N; q fragments in registers)
+//   online softmax per head on the accumulator fragments (scores in log2 units)
+//   O^T[d x 8] += V^T[d x 16] . P^T[16 x 8]            (V^T via ldmatrix.trans; P split
+//                                                         into bf16 hi + lo halves, so the
+//                                                         weights keep ~16 mantissa bits)
+// Each warp writes its partial {m, l, acc[d]} per head; the last split of the unit
+// merges all partials by log-sum-exp.
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+// 16-byte async copy; src_bytes = 0 fills the destination with zeros.
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
+               : "memory");
+}
+
+// bf16 pair (lo element in the low half) of two floats, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+template <int D, int NBUF>
+__device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint16_t* __restrict__ q,
                              float* __restrict__ out, int64_t u, int split, int gtid) {
-  constexpr int VPR = D / 4;
-  constexpr int NG = AttSmem<D>::NG;
+  constexpr int VPR = D / 4;  // 16-byte vectors per K|V record
+  constexpr int KS = D / 16;  // k-steps of S = K Q^T, also m-blocks of O^T
+  constexpr int WROWS = kSplitRows / kCompWarps;
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
   const int l = (int)(u / ((int64_t)s.Hkv * s.B));
   const int G = s.G;
-  const int warp = gtid >> 5, lane = gtid & 31;
+  const int warp = gtid >> 5, lane = gtid & 31, gid = lane >> 2, tig = lane & 3;
   const int64_t N = s.ntok[b];
   const int64_t k = s.kcount[b];
-  const int64_t r0 = (int64_t)split * s.split_rows;
-  const int64_t r1 = (r0 + s.split_rows < k) ? r0 + s.split_rows : k;
+  const int64_t r0 = (int64_t)split * kSplitRows + (int64_t)warp * WROWS;
+  const int64_t r1 = (r0 + WROWS < k) ? r0 + WROWS : k;
   const bool persistent = s.decision[u] == CLO_DEC_PERSIST;
   const int32_t* ix = s.idx + u * s.kmax;
   const uint4* src;
@@ -361,112 +392,169 @@ __device__ void attend_split(const DevState& s, AttSmem<D>& sm, const uint16_t* 
   } else {
     src = reinterpret_cast<const uint4*>(s.slots) + (u * s.kmax) * VPR;
   }
+  // Q^T fragments (B operand): head gid, dims 2*tig (+1, +8, +9) of each k-step
+  uint32_t qb[KS][2];
+  {
+    const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (gid < G) {
+        qb[ks][0] = *reinterpret_cast<const uint32_t*>(qg + gid * D + ks * 16 + 2 * tig);
+        qb[ks][1] = *reinterpret_cast<const uint32_t*>(qg + gid * D + ks * 16 + 2 * tig + 8);
+      } else {
+        qb[ks][0] = qb[ks][1] = 0u;
+      }
+    }
+  }
   const float qscale = 1.4426950408889634f * rsqrtf((float)D);  // scores in log2 units
-  const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * D;
-  for (int e = gtid; e < G * D; e += kCompThreads) sm.qs[e / D][e % D] = bf16_bits_to_f32(qg[e]) * qscale;
-  if (gtid < kMaxG) {
-    sm.m_run[gtid] = -INFINITY;
-    sm.l_run[gtid] = 0.f;
-  }
-  float acc[kMaxG];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;      // heads 2*tig, 2*tig+1
+  float acc[KS][4];
 #pragma unroll
-  for (int g = 0; g < kMaxG; ++g) acc[g] = 0.f;
-  const int dj = gtid % D;
-  const int rg = gtid / D;
-  comp_bar();
+  for (int mb = 0; mb < KS; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
 
-  for (int64_t rb = r0; rb < r1; rb += kAttTile) {
-    const int nrows = (int)((r1 - rb) < kAttTile ? (r1 - rb) : kAttTile);
-    for (int e = gtid; e < nrows * VPR; e += kCompThreads) {
-      const int r = e / VPR, c = e % VPR;
-      int64_t srow = rb + r;
-      if (persistent) {
-        srow = __ldcg(ix + rb + r);
-        if (srow < 0 || srow >= N) {
-          atomicOr(s.err, kErrBounds);
-          srow = 0;
-        }
-      }
-      cp_async16(&sm.rows[r][c * 8], src + srow * VPR + c);
+  // copy layout: lane -> row lane % 16, half lane / 16 of the record's vectors
+  const int cr = lane & 15, chalf = lane >> 4;
+  auto row_of = [&](int64_t rb) -> int64_t {
+    const int64_t t = rb + cr;
+    if (t >= r1) return 0;
+    if (!persistent) return t;
+    int64_t v = __ldcg(ix + t);
+    if (v < 0 || v >= N) {
+      atomicOr(s.err, kErrBounds);
+      v = 0;
     }
+    return v;
+  };
+  auto issue = [&](int64_t rb, int buf, int64_t srow) {
+    const uint32_t bytes = rb + cr < r1 ? 16u : 0u;
+    const uint4* sp = src + srow * VPR + chalf * (VPR / 2);
+    uint16_t* dp = &sm.rows[warp][buf][cr][chalf * (VPR / 2) * 8];
+#pragma unroll
+    for (int c = 0; c < VPR / 2; ++c) cp_async16_zfill(dp + c * 8, sp + c, bytes);
     cp_async_commit();
-    cp_async_wait<0>();
-    comp_bar();
-    for (int p = gtid; p < G * kAttTile; p += kCompThreads) {
-      const int g = p / kAttTile, r = p % kAttTile;
-      float dot = -INFINITY;
-      if (r < nrows) {
-        dot = 0.f;
-        const uint4* kr = reinterpret_cast<const uint4*>(&sm.rows[r][0]);
-#pragma unroll 4
-        for (int i = 0; i < D / 8; ++i) {
-          const uint4 w = kr[i];
-          const float4 qa = *reinterpret_cast<const float4*>(&sm.qs[g][8 * i]);
-          const float4 qb = *reinterpret_cast<const float4*>(&sm.qs[g][8 * i + 4]);
-          dot = fmaf(qa.x, __uint_as_float(w.x << 16), dot);
-          dot = fmaf(qa.y, __uint_as_float(w.x & 0xffff0000u), dot);
-          dot = fmaf(qa.z, __uint_as_float(w.y << 16), dot);
-          dot = fmaf(qa.w, __uint_as_float(w.y & 0xffff0000u), dot);
-          dot = fmaf(qb.x, __uint_as_float(w.z << 16), dot);
-          dot = fmaf(qb.y, __uint_as_float(w.z & 0xffff0000u), dot);
-          dot = fmaf(qb.z, __uint_as_float(w.w << 16), dot);
-          dot = fmaf(qb.w, __uint_as_float(w.w & 0xffff0000u), dot);
+  };
+  if (r0 < r1) {
+    int64_t nxt = row_of(r0);
+    if (NBUF == 2) {
+      issue(r0, 0, nxt);
+      nxt = row_of(r0 + 16);
+    }
+    int ci = 0;
+    for (int64_t rb = r0; rb < r1; rb += 16, ++ci) {
+      const int buf = NBUF == 2 ? (ci & 1) : 0;
+      if (NBUF == 2) {
+        if (rb + 16 < r1) {
+          issue(rb + 16, buf ^ 1, nxt);
+          nxt = row_of(rb + 32);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+      } else {
+        issue(rb, 0, nxt);
+        nxt = row_of(rb + 16);  // index load overlaps the copy
+        cp_async_wait<0>();
+      }
+      __syncwarp();
+      uint16_t(*rows)[AttSmem<D, NBUF>::ROWW] = sm.rows[warp][buf];
+      const int nrows = (int)((r1 - rb) < 16 ? (r1 - rb) : 16);
+      // S = K Q^T
+      float sf[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ac = 8 * (lane >> 4);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(a, &rows[ar][ks * 16 + ac]);
+          mma_bf16_16816(sf, a, qb[ks]);
         }
       }
-      sm.sc[g][r] = dot;
-    }
-    comp_bar();
-    for (int g = warp; g < G; g += kCompWarps) {
-      const float v = sm.sc[g][lane];
-      const float mx = warp_max(v);
-      const float mo = sm.m_run[g];
-      const float mn = fmaxf(mo, mx);
-      const float pv = exp2f(v - mn);
-      const float ps = warp_sum(pv);
-      sm.sc[g][lane] = pv;
-      if (lane == 0) {
-        const float a = exp2f(mo - mn);
-        sm.alpha[g] = a;
-        sm.l_run[g] = sm.l_run[g] * a + ps;
-        sm.m_run[g] = mn;
+      // rows gid (sf[0], sf[1]) and gid + 8 (sf[2], sf[3]); heads 2*tig, 2*tig+1
+      const float s00 = gid < nrows ? sf[0] * qscale : -INFINITY;
+      const float s01 = gid < nrows ? sf[1] * qscale : -INFINITY;
+      const float s10 = gid + 8 < nrows ? sf[2] * qscale : -INFINITY;
+      const float s11 = gid + 8 < nrows ? sf[3] * qscale : -INFINITY;
+      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-    }
-    comp_bar();
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
+      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+      float rs0 = p00 + p10, rs1 = p01 + p11;
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g)
-      if (g < G) acc[g] *= sm.alpha[g];
-    for (int r = rg; r < nrows; r += NG) {
-      const float v = bf16_bits_to_f32(sm.rows[r][D + dj]);
+      for (int o = 4; o < 32; o <<= 1) {
+        rs0 += __shfl_xor_sync(0xffffffffu, rs0, o);
+        rs1 += __shfl_xor_sync(0xffffffffu, rs1, o);
+      }
+      l0 = l0 * al0 + rs0;
+      l1 = l1 * al1 + rs1;
+      m0 = mn0;
+      m1 = mn1;
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g)
-        if (g < G) acc[g] = fmaf(sm.sc[g][r], v, acc[g]);
+      for (int mb = 0; mb < KS; ++mb) {
+        acc[mb][0] *= al0;
+        acc[mb][2] *= al0;
+        acc[mb][1] *= al1;
+        acc[mb][3] *= al1;
+      }
+      // P^T fragments (B operand): rows 2*tig, 2*tig+1, 2*tig+8, 2*tig+9 of head gid.
+      // P[r][hd] sits in lane 4*(r%8) + hd/2: element hd%2 of (p00,p01) for r < 8, of
+      // (p10,p11) for r >= 8.
+      const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
+      const bool odd = gid & 1;
+      const float xa0 = __shfl_sync(0xffffffffu, p00, sa), xa1 = __shfl_sync(0xffffffffu, p01, sa);
+      const float xb0 = __shfl_sync(0xffffffffu, p00, sb), xb1 = __shfl_sync(0xffffffffu, p01, sb);
+      const float ya0 = __shfl_sync(0xffffffffu, p10, sa), ya1 = __shfl_sync(0xffffffffu, p11, sa);
+      const float yb0 = __shfl_sync(0xffffffffu, p10, sb), yb1 = __shfl_sync(0xffffffffu, p11, sb);
+      const float pr0 = odd ? xa1 : xa0, pr1 = odd ? xb1 : xb0;  // rows 2*tig, 2*tig+1
+      const float pr8 = odd ? ya1 : ya0, pr9 = odd ? yb1 : yb0;  // rows 2*tig+8, 2*tig+9
+      uint32_t bh[2], bl[2];
+      bh[0] = pack_bf16(pr0, pr1);
+      bh[1] = pack_bf16(pr8, pr9);
+      bl[0] = pack_bf16(pr0 - bf16_round(pr0), pr1 - bf16_round(pr1));
+      bl[1] = pack_bf16(pr8 - bf16_round(pr8), pr9 - bf16_round(pr9));
+      // O^T += V^T P^T
+      {
+        const int vr = (lane & 7) + 8 * (lane >> 4), vc = 8 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int mb = 0; mb < KS; ++mb) {
+          uint32_t a[4];
+          ldsm_x4_trans(a, &rows[vr][D + mb * 16 + vc]);
+          mma_bf16_16816(acc[mb], a, bh);
+          mma_bf16_16816(acc[mb], a, bl);
+        }
+      }
+      __syncwarp();  // this buffer is refilled by a later chunk
     }
-    comp_bar();
   }
 
-  if (NG > 1) {
+  // this warp's partial: {m, l, acc[d]} for heads 2*tig, 2*tig+1 (< G)
+  float* part = s.part + (((u * s.nsplit + split) * kCompWarps + warp) * G) * (D + 2);
+  const int h0 = 2 * tig, h1 = 2 * tig + 1;
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g)
-      if (g < G) sm.red[rg][g][dj] = acc[g];
-    comp_bar();
-  }
-  float* part = s.part + ((u * s.nsplit + split) * G) * (D + 2);
-  if (gtid < D) {
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      if (g < G) {
-        float a = acc[g];
-        if (NG > 1) {
-          a = 0.f;
-          for (int r = 0; r < NG; ++r) a += sm.red[r][g][gtid];
-        }
-        part[g * (D + 2) + 2 + gtid] = a;
-      }
+  for (int mb = 0; mb < KS; ++mb) {
+    if (h0 < G) {
+      part[h0 * (D + 2) + 2 + mb * 16 + gid] = acc[mb][0];
+      part[h0 * (D + 2) + 2 + mb * 16 + gid + 8] = acc[mb][2];
+    }
+    if (h1 < G) {
+      part[h1 * (D + 2) + 2 + mb * 16 + gid] = acc[mb][1];
+      part[h1 * (D + 2) + 2 + mb * 16 + gid + 8] = acc[mb][3];
     }
   }
-  if (gtid < G) {
-    part[gtid * (D + 2) + 0] = sm.m_run[gtid];
-    part[gtid * (D + 2) + 1] = sm.l_run[gtid];
+  if (gid == 0) {
+    if (h0 < G) {
+      part[h0 * (D + 2) + 0] = m0;
+      part[h0 * (D + 2) + 1] = l0;
+    }
+    if (h1 < G) {
+      part[h1 * (D + 2) + 0] = m1;
+      part[h1 * (D + 2) + 1] = l1;
+    }
   }
   __threadfence();
   comp_bar();
@@ -477,32 +565,58 @@ __device__ void attend_split(const DevState& s, AttSmem<D>& sm, const uint16_t* 
   comp_bar();
   if (!sm.last) return;
   __threadfence();
-  const float* pu = s.part + (u * s.nsplit) * G * (D + 2);
+  // merge: per head, weights w_sp = exp2(m_sp - M) of all partials (into shared memory,
+  // reusing the row buffers), then out[j] = sum_sp w_sp acc_sp[j] / sum_sp w_sp l_sp
+  const int np = s.nsplit * kCompWarps;
+  const float* pu = s.part + (u * np) * G * (D + 2);
   float* og = out + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * D;
-  for (int e = gtid; e < G * D; e += kCompThreads) {
-    const int g = e / D, j = e % D;
-    float M = -INFINITY;
-    for (int sp = 0; sp < s.nsplit; ++sp) M = fmaxf(M, __ldcg(pu + (sp * G + g) * (D + 2)));
-    float Lsum = 0.f, O = 0.f;
-    for (int sp = 0; sp < s.nsplit; ++sp) {
+  float* w = reinterpret_cast<float*>(&sm.rows[0][0][0][0]);  // np floats
+  for (int g = 0; g < G; ++g) {
+    float mx = -INFINITY;
+    for (int sp = gtid; sp < np; sp += kCompThreads) {
       const float* ps = pu + (sp * G + g) * (D + 2);
-      const float ls = __ldcg(ps + 1);
-      if (ls > 0.f) {
-        const float w = exp2f(__ldcg(ps) - M);
-        Lsum = fmaf(ls, w, Lsum);
-        O = fmaf(__ldcg(ps + 2 + j), w, O);
-      }
+      if (__ldcg(ps + 1) > 0.f) mx = fmaxf(mx, __ldcg(ps));
     }
-    og[g * D + j] = O / Lsum;
+    mx = warp_max(mx);
+    if (lane == 0) sm.red[warp] = mx;
+    comp_bar();
+    const float M = fmaxf(fmaxf(sm.red[0], sm.red[1]), fmaxf(sm.red[2], sm.red[3]));
+    float ls = 0.f;
+    for (int sp = gtid; sp < np; sp += kCompThreads) {
+      const float* ps = pu + (sp * G + g) * (D + 2);
+      const float lsp = __ldcg(ps + 1);
+      const float ww = lsp > 0.f ? exp2f(__ldcg(ps) - M) : 0.f;
+      w[sp] = ww;
+      ls = fmaf(lsp, ww, ls);
+    }
+    ls = warp_sum(ls);
+    comp_bar();  // everyone has read sm.red (max)
+    if (lane == 0) sm.red[warp] = ls;
+    comp_bar();
+    const float Lsum = sm.red[0] + sm.red[1] + sm.red[2] + sm.red[3];
+    for (int j = gtid; j < D; j += kCompThreads) {
+      float O = 0.f;
+      for (int sp = 0; sp < np; ++sp) {
+        const float ww = w[sp];
+        if (ww != 0.f) O = fmaf(__ldcg(pu + (sp * G + g) * (D + 2) + 2 + j), ww, O);
+      }
+      og[g * D + j] = O / Lsum;
+    }
+    comp_bar();  // w and sm.red are reused by the next head
   }
   if (gtid == 0) s.unit_done[u] = 0u;
 }
 
 // ---- fetch warps -----------------------------------------------------------------------
-template <int D>
-__device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int lane) {
+// A fetch item is one chunk of kChunkRows selected rows of a missed unit.  The chunk's
+// indices are checked and staged in shared memory first, so every round trip to host
+// memory is a single dependent load; each round keeps kFetchUnroll 16-byte loads per
+// lane in flight (with d = 128 one warp-wide load is one whole 512-byte K|V record).
+template <int D, int FU>
+__device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int lane, int32_t* sidx) {
+  constexpr int kFetchUnroll = FU;
   constexpr int VPR = D / 4;  // 16-byte vectors per K|V record
-  const int NS = s.nsplit, RS = s.split_rows, L = s.L, BH = s.B * s.Hkv;
+  const int NS = s.nchunk, RS = kChunkRows, L = s.L, BH = s.B * s.Hkv;
   const int64_t n_items = (int64_t)n_miss * NS;
   while (true) {
     unsigned item = 0;
@@ -516,52 +630,70 @@ __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int 
     const int64_t k = s.kcount[b];
     const int64_t N = s.ntok[b];
     const int64_t r0 = (int64_t)c * RS;
-    const int64_t r1 = (r0 + RS < k) ? r0 + RS : k;
-    if (r0 < r1) {
-      // missed units were selected by the launch before this one
-      if (lane == 0 && s.timeline) atomicCAS(&s.timeline[TL_FETCH_FIRST], 0ull, global_timer_ns());
+    const int nr = (int)((r0 + RS < k) ? RS : (k - r0 > 0 ? k - r0 : 0));
+    if (nr > 0) {
+      if (lane == 0) {  // the unit's selection: compute groups, earlier in their queue
+        const uint64_t tw = s.timeline ? global_timer_ns() : 0;
+        wait_flag(&s.sel_cnt[u], (uint32_t)s.nch, s);
+        if (s.timeline) {
+          const uint64_t t1 = global_timer_ns();
+          atomicAdd(&s.timeline[TL_FETCH_WAIT_NS], t1 - tw);
+          atomicCAS(&s.timeline[TL_FETCH_FIRST], 0ull, t1);
+        }
+      }
+      __syncwarp();
+      const int32_t* ix = s.idx + u * s.kmax + r0;
+      for (int i = lane; i < nr; i += 32) {
+        int32_t t = __ldcg(ix + i);
+        if (t < 0 || (int64_t)t >= N) {
+          atomicOr(s.err, kErrBounds);
+          t = -1;
+        }
+        sidx[i] = t;
+      }
+      __syncwarp();
       const uint4* pool = reinterpret_cast<const uint4*>(s.pool) + u * s.Nmax * VPR;
-      uint4* slot = reinterpret_cast<uint4*>(s.slots) + u * s.kmax * VPR;
-      const int32_t* ix = s.idx + u * s.kmax;
-      const int64_t total = (r1 - r0) * VPR;
-      for (int64_t e0 = lane; e0 < total; e0 += 32 * kFetchUnroll) {
+      uint4* slot = reinterpret_cast<uint4*>(s.slots) + (u * s.kmax + r0) * VPR;
+      const int total = nr * VPR;
+      for (int e0 = lane; e0 < total; e0 += 32 * kFetchUnroll) {
         uint4 v[kFetchUnroll];
 #pragma unroll
         for (int j = 0; j < kFetchUnroll; ++j) {
-          const int64_t e = e0 + 32 * j;
+          const int e = e0 + 32 * j;
+          v[j] = make_uint4(0, 0, 0, 0);
           if (e < total) {
-            const int64_t t = __ldcg(ix + r0 + e / VPR);
-            if (t >= 0 && t < N) {
-              v[j] = ld_nc_v4(pool + t * VPR + (e % VPR));
-            } else {
-              atomicOr(s.err, kErrBounds);
-              v[j] = make_uint4(0, 0, 0, 0);
-            }
+            const int t = sidx[e / VPR];
+            if (t >= 0) v[j] = ld_nc_v4(pool + (int64_t)t * VPR + (e % VPR));
           }
         }
 #pragma unroll
         for (int j = 0; j < kFetchUnroll; ++j) {
-          const int64_t e = e0 + 32 * j;
-          if (e < total) slot[r0 * VPR + e] = v[j];
+          const int e = e0 + 32 * j;
+          if (e < total) slot[e] = v[j];
         }
       }
     }
     __threadfence();
-    __syncwarp();
+    __syncwarp();  // also: sidx is rewritten by the next item
     if (lane == 0 && l != s.drop_flag_layer) red_release_add_u32(&s.ready[u * NS + c], 1u);
     if (lane == 0 && s.timeline) atomicMax(&s.timeline[TL_FETCH_END], global_timer_ns());
   }
 }
 
 // ---- the kernel ------------------------------------------------------------------------
-template <int D, int G>
-__global__ void __launch_bounds__(kFThreads, 6) k_step_fused(DevState s, const uint16_t* __restrict__ q,
-                                                             float* __restrict__ out) {
+// FW fetch warps + one compute group per CTA; MINB CTAs per SM; NBUF row buffers per
+// compute warp.
+template <int D, int G, int FW, int MINB, int NBUF, int FU = kFetchUnroll>
+__global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
+    k_step_fused(DevState s, const uint16_t* __restrict__ q, float* __restrict__ out) {
+  using Smem = CompSmem<D, NBUF>;
   __shared__ int pre[3][kMaxLayers + 1];  // hit, persistent, missed lists
   __shared__ long long sec_start[6];
-  __shared__ uint64_t ring_bar[kSelStages];
   __shared__ int s_item;
-  __shared__ __align__(128) CompSmem<D> sm;
+  __shared__ unsigned long long s_t0;  // start of the group's item (timing mode)
+  __shared__ int32_t fidx[FW][kChunkRows];
+  extern __shared__ __align__(128) unsigned char dsm[];
+  Smem& sm = *reinterpret_cast<Smem*>(dsm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = s.L;
   if (tid == 0) {
@@ -573,25 +705,22 @@ __global__ void __launch_bounds__(kFThreads, 6) k_step_fused(DevState s, const u
         a[j] += s.lcnt[j * L + l];
         pre[j][l + 1] = a[j];
       }
-    // compute queue: selections of the persistent units (per layer: the layer's chunk
-    // scores, finalizes, chunk compactions), then attention splits of reused,
-    // persistent and missed units
-    const long long nh = a[0], np = a[1], nm = a[2], SB = 2LL * s.nch + 1, NS = s.nsplit;
-    const long long size[5] = {0, np * SB, nh * NS, np * NS, nm * NS};
+    // compute queue: selection chunks of the missed units, then of the persistent units
+    // (layer by layer, the chunks of a unit next to each other), then attention splits
+    // of reused, persistent and missed units
+    const long long nh = a[0], np = a[1], nm = a[2], NC = s.nch, NS = s.nsplit;
+    const long long size[5] = {nm * NC, np * NC, nh * NS, np * NS, nm * NS};
     sec_start[0] = 0;
     for (int i = 0; i < 5; ++i) sec_start[i + 1] = sec_start[i] + size[i];
-    for (int i = 0; i < kSelStages; ++i) mbar_init(&ring_bar[i], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (warp < kFetchWarps) {
-    fetch_role<D>(s, pre[2], pre[2][L], lane);
+  if (warp < FW) {
+    fetch_role<D, FU>(s, pre[2], pre[2][L], lane, fidx[warp]);
     return;  // no block-wide barrier after this point
   }
-  const int gtid = tid - 32 * kFetchWarps;
+  const int gtid = tid - 32 * FW;
   const int BH = s.B * s.Hkv;
   const int NC = s.nch;
-  Ring ring{ring_bar, 0u};
   const long long total = sec_start[5];
   while (true) {
     if (gtid == 0) s_item = (int)atomicAdd(&s.queue[1], 1u);
@@ -604,63 +733,77 @@ __global__ void __launch_bounds__(kFThreads, 6) k_step_fused(DevState s, const u
     const int list = (sec == 0 || sec == 4) ? 2 : ((sec == 1 || sec == 3) ? 1 : 0);
     const int* pl = pre[list];
     const int32_t* lst = list == 2 ? s.miss_list : (list == 1 ? s.pers_list : s.hit_list);
-    if (sec <= 1) {  // selection block of one layer
-      const long long SB = 2LL * NC + 1;
-      const int l = layer_of(pl, L, (int)(j / SB));
-      const int n = pl[l + 1] - pl[l];
-      const long long r = j - (long long)pl[l] * SB;
-      const int32_t* ll = lst + (int64_t)l * BH;
-      if (r < (long long)n * NC) {
-        sel_score<G>(s, sm.sel, ring, ll[r / NC], (int)(r % NC), gtid);
-      } else if (r < (long long)n * NC + n) {
-        sel_finalize<G>(s, sm.sel, ll[r - (long long)n * NC], gtid);
-      } else {
-        const long long r2 = r - (long long)n * NC - n;
-        sel_compact<G>(s, sm.sel, ring, ll[r2 / NC], (int)(r2 % NC), gtid);
+    if (s.timeline && gtid == 0) s_t0 = global_timer_ns();
+    if (sec <= 1) {  // selection chunk
+      const int p = (int)(j / NC), c = (int)(j % NC);
+      const int l = layer_of(pl, L, p);
+      const int64_t u = lst[(int64_t)l * BH + (p - pl[l])];
+      sel_chunk<G>(s, sm.sel, u, c, gtid);
+      if (s.timeline && gtid == 0) {
+        const uint64_t t1 = global_timer_ns();
+        atomicMax(&s.timeline[sec == 0 ? TL_SEL_MISS_END : TL_SEL_PERS_END], t1);
+        atomicAdd(&s.timeline[TL_SEL_SUM_NS], t1 - s_t0);
+        atomicAdd(&s.timeline[TL_SEL_ITEMS], 1ull);
       }
-      if (s.timeline && gtid == 0) atomicMax(&s.timeline[sec == 0 ? TL_SEL_MISS_END : TL_SEL_PERS_END], global_timer_ns());
     } else {  // attention split
       const int p = (int)(j / s.nsplit), c = (int)(j % s.nsplit);
       const int l = layer_of(pl, L, p);
       const int64_t u = lst[(int64_t)l * BH + (p - pl[l])];
       const int b = (int)((u / s.Hkv) % s.B);
-      const int64_t r0 = (int64_t)c * s.split_rows;
-      if (s.timeline && gtid == 0) atomicCAS(&s.timeline[TL_ATT_FIRST], 0ull, global_timer_ns());
+      const int64_t r0 = (int64_t)c * kSplitRows;
+      if (s.timeline && gtid == 0) atomicCAS(&s.timeline[TL_ATT_FIRST], 0ull, s_t0);
       if (sec == 3) {
         if (gtid == 0) wait_flag(&s.sel_cnt[u], (uint32_t)NC, s);
         comp_bar();
       } else if (sec == 4 && r0 < s.kcount[b]) {
         if (gtid == 0) {
-          const uint64_t t0 = s.timeline ? global_timer_ns() : 0;
-          wait_flag(&s.ready[u * s.nsplit + c], 1u, s);
-          if (s.timeline) atomicAdd(&s.timeline[TL_ATT_WAIT_NS], global_timer_ns() - t0);
+          constexpr int kPer = kSplitRows / kChunkRows;  // the fetch chunks this split reads
+          for (int fc = c * kPer; fc < (c + 1) * kPer && (int64_t)fc * kChunkRows < s.kcount[b]; ++fc)
+            wait_flag(&s.ready[u * s.nchunk + fc], 1u, s);
+          if (s.timeline) atomicAdd(&s.timeline[TL_ATT_WAIT_NS], global_timer_ns() - s_t0);
         }
         comp_bar();
       }
-      attend_split<D>(s, sm.att, q, out, u, c, gtid);
-      if (s.timeline && gtid == 0) atomicMax(&s.timeline[TL_COMP_END], global_timer_ns());
+      attend_split<D, NBUF>(s, sm.att, q, out, u, c, gtid);
+      if (s.timeline && gtid == 0) {
+        const uint64_t t1 = global_timer_ns();
+        atomicMax(&s.timeline[TL_COMP_END], t1);
+        atomicAdd(&s.timeline[TL_ATT_SUM_NS], t1 - s_t0);
+        atomicAdd(&s.timeline[TL_ATT_ITEMS], 1ull);
+      }
     }
     comp_bar();
   }
 }
 
-template <int D, int G>
+template <int D, int G, int FW, int MINB, int NBUF, int FU>
 int fused_grid() {
   static int grid = 0;
   if (grid == 0) {
+    auto kern = k_step_fused<D, G, FW, MINB, NBUF, FU>;
+    const int smem = (int)sizeof(CompSmem<D, NBUF>);
     int dev = 0, sms = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_step_fused<D, G>, kFThreads, 0);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * (FW + kCompWarps), smem);
     grid = sms * (per_sm > 0 ? per_sm : 1);
   }
   return grid;
 }
 
+template <int D, int G, int FW, int MINB, int NBUF, int FU = kFetchUnroll>
+cudaError_t launch_v(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
+  k_step_fused<D, G, FW, MINB, NBUF, FU><<<fused_grid<D, G, FW, MINB, NBUF, FU>(), 32 * (FW + kCompWarps),
+                                       sizeof(CompSmem<D, NBUF>), st>>>(s, q, out);
+  return cudaGetLastError();
+}
+
 template <int D, int G>
 cudaError_t launch_dg(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
-  k_step_fused<D, G><<<fused_grid<D, G>(), kFThreads, 0, st>>>(s, q, out);
-  return cudaGetLastError();
+  // the selection's waits need all chunks of a unit running at once
+  if (fused_grid<D, G, 1, 3, 2, kFetchUnroll>() < s.nch) return cudaErrorInvalidConfiguration;
+  return launch_v<D, G, 1, 3, 2>(s, q, out, st);
 }
 
 template <int D>
@@ -701,7 +844,7 @@ __global__ void k_resident_fill(DevState s, int64_t t0, int64_t t1) {
 }  // namespace
 
 cudaError_t launch_step_fused(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
-  if (s.L > kMaxLayers || s.nch > kMaxChunks || s.nbp > kNBPad) return cudaErrorInvalidValue;
+  if (s.L > kMaxLayers || s.nbp > kNBPad) return cudaErrorInvalidValue;
   if (s.d == 128) return launch_d<128>(s, q, out, st);
   if (s.d == 64) return launch_d<64>(s, q, out, st);
   return cudaErrorInvalidValue;

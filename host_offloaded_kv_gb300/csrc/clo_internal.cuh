@@ -6,6 +6,7 @@
 //   qcodes     (HBM)                   uint4 [L][B][Hq]              query codes of the step
 //   qcache     (HBM)                   bf16 [U][G*d]                 query at the last refresh
 //   idx        (HBM)                   int32 [U][kmax]               selection, ascending
+//   unit_hist  (HBM)                   uint32 [U][nbp]               score histogram of the step
 //   slots      (HBM)                   bf16 [U][kmax][K | V]         on-GPU cache of fetched rows
 //   resident   (HBM)                   bf16 [L][B][P][Nmax][K | V]   persistent heads' full K/V
 #pragma once
@@ -68,19 +69,21 @@ struct DevState {
   unsigned long long* total_ctr;// [C_NUM][kCtrLanes] since init
   uint32_t* err;                // error word
   uint32_t* unit_done;          // [U] split counters of the attention combine
-  float* part;                  // attention partials [U][nsplit][G][d + 2]
-  int nsplit;                   // attention splits per unit
-  int split_rows;               // rows per split
-  uint32_t* ready;              // [U][nsplit] fetch-ready flag per row chunk (zeroed per step)
+  float* part;                  // attention partials [U][nsplit][kPartsPerSplit][G][d + 2]
+  int nsplit;                   // attention splits per unit (kSplitRows rows each)
+  int nchunk;                   // fetch chunks per unit (kChunkRows rows each)
+  uint32_t* ready;              // [U][nchunk] fetch-ready flag per row chunk (zeroed per step)
   int* lcnt;                    // [3L] per-layer list lengths: hit, persistent, missed (zeroed per step)
   int32_t* hit_list;            // [L][B*Hkv] units reusing their selection, per layer
   int32_t* pers_list;           // [L][B*Hkv] persistent units, per layer
   int32_t* miss_list;           // [L][B*Hkv] missed units, per layer
   unsigned* queue;              // [2] work counters: fetch, compute (zeroed per step)
-  uint32_t* sel_hist;           // [U][nch][nbp] score histogram of each selection chunk
-  int4* sel_meta;               // [U][nch] {output offset, tie quota, threshold T, 0}
-  uint32_t* score_done;         // [U] chunks scored (zeroed per step)
-  uint32_t* fin_done;           // [U] threshold known (zeroed per step)
+  uint32_t* unit_hist;          // [U][nbp] score histogram of each unit being selected (zeroed per step)
+  int2* sel_meta;               // [U][nch] {count above T, count at T} of each selection chunk
+  int2* sel_thr;                // [U] {threshold score T, count above T}
+  uint32_t* score_done;         // [U] chunks whose histogram is merged (zeroed per step)
+  uint32_t* fin_done;           // [U] threshold published (zeroed per step)
+  uint32_t* cnt_done;           // [U] chunk counts published (zeroed per step)
   uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
   int nch;                      // selection chunks per unit = ceil(Nmax / kSelChunk)
   int nbp;                      // histogram bins per chunk, padded (>= 128*G + 1)
@@ -94,17 +97,24 @@ constexpr int kMaxLayers = 256;
 // timeline slots of the fused step kernel (ns of %globaltimer; first = first writer)
 enum Timeline : int {
   TL_START = 0,          // first CTA started
-  TL_SEL_MISS_END = 1,   // last selection item of a missed unit finished
-  TL_SEL_PERS_END = 2,   // last selection item of a persistent unit finished
+  TL_SEL_MISS_END = 1,   // last selection chunk of a missed unit finished
+  TL_SEL_PERS_END = 2,   // last selection chunk of a persistent unit finished
   TL_FETCH_FIRST = 3,    // first fetch chunk could start copying
   TL_FETCH_END = 4,      // last fetch chunk released
   TL_ATT_FIRST = 5,      // first attention split started
   TL_COMP_END = 6,       // last attention split finished
   TL_FETCH_WAIT_NS = 7,  // summed waits of fetch warps on selections
   TL_ATT_WAIT_NS = 8,    // summed waits of attention groups on fetch flags
+  TL_SEL_SUM_NS = 9,     // summed durations of selection chunks
+  TL_SEL_ITEMS = 10,     // selection chunks run
+  TL_ATT_SUM_NS = 11,    // summed durations of attention splits (waits included)
+  TL_ATT_ITEMS = 12,     // attention splits run
   kTimelineSlots = 16
 };
 constexpr int kSelChunk = 8192;  // tokens per selection chunk
+constexpr int kPartsPerSplit = 4; // attention partials per split (one per compute warp)
+constexpr int kSplitRows = 1024;  // selected rows per attention split
+constexpr int kChunkRows = 256;   // selected rows per fetch chunk (one ready flag each)
 constexpr int kNBPad = 1056;     // >= 128 * kMaxG + 1, multiple of 32
 
 __host__ __device__ inline int64_t unit_of(const DevState& s, int l, int b, int h) {
@@ -220,8 +230,6 @@ cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_
                              cudaStream_t st);
 cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st);
 cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st);
-cudaError_t launch_select(const DevState& s, int cluster, int64_t chunk, cudaStream_t st);
-size_t select_smem_bytes(int G, int64_t chunk);
 cudaError_t launch_step_fused(const DevState& s, const uint16_t* q, float* out, cudaStream_t st);
 cudaError_t launch_resident_fill(const DevState& s, int64_t t0, int64_t t1, cudaStream_t st);
 cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,

@@ -110,14 +110,14 @@ typedef struct clo_stats_t {
   int64_t timeouts;          /* ready-flag waits that gave up */
   int64_t last_hit, last_miss, last_persist, last_host_bytes, last_hbm_bytes_alg;
   int32_t warmup_done;       /* 1 once thresholds and persistent heads are fixed */
-  /* timing != 0: CUDA-event times of the three launches of a step (decide = reuse
-   * test and query hashing; select = scoring and top-k of the missed units; fused =
-   * selection of the persistent units, host-row fetch and sparse attention in one
-   * persistent kernel) and of the whole step, for the last step and summed over the
-   * timed_steps steps since the previous clo_stats call. */
+  /* timing != 0: CUDA-event times of the two launches of a step (decide = reuse
+   * test and query hashing; fused = top-k selection of the missed and persistent
+   * units, host-row fetch and sparse attention in one persistent kernel) and of the
+   * whole step, for the last step and summed over the timed_steps steps since the
+   * previous clo_stats call. */
   int32_t timed_steps;
-  float last_ms_decide, last_ms_select, last_ms_fused, last_ms_total;
-  double sum_ms_decide, sum_ms_select, sum_ms_fused, sum_ms_total;
+  float last_ms_decide, last_ms_fused, last_ms_total;
+  double sum_ms_decide, sum_ms_fused, sum_ms_total;
 } clo_stats_t;
 
 /* Fill *cfg with defaults (shapes zero; topk_ratio 0.1; warmup_steps 16;
@@ -181,11 +181,13 @@ CLO_API const char* clo_last_error(void);
  *   CLO_DBG_COS         fp32 [L][B][Hkv] cosines of the last step (NaN if none)
  *   CLO_DBG_TIMELINE    uint64 [16] %globaltimer stamps (ns) of the last step's fused
  *                       kernel, timing mode only (zeros otherwise): [0] start, [1] last
- *                       selection of a missed unit done, [2] last selection of a
- *                       persistent unit done, [3] first fetch chunk able to start,
+ *                       selection chunk of a missed unit done, [2] last selection chunk
+ *                       of a persistent unit done, [3] first fetch chunk able to start,
  *                       [4] last fetch chunk done, [5] first attention split, [6] last
  *                       attention split done, [7] summed fetch waits on selections,
- *                       [8] summed attention waits on fetch flags
+ *                       [8] summed attention waits on fetch flags, [9] summed durations
+ *                       of selection chunks, [10] their number, [11] summed durations
+ *                       of attention splits, [12] their number
  * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,
