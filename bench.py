@@ -330,7 +330,7 @@ def run_gb300(args, rank, world, local_rank):
              "+ attention row reads + slot writes) / kernel time")
     dom = "fused"
     dk = kern[dom]
-    traffic = traffic_from_profiles(dom, w.name)
+    traffic = traffic_from_profiles("k_step_fused", w.name)
     roofline = {"kernel": "k_step_fused",
                 "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"], "unit": "GB/s",
                 "frac": (dk["achieved_gbs"] / dk["peak_gbs"]) if dk["achieved_gbs"] else None,

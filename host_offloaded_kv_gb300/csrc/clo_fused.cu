@@ -57,8 +57,9 @@ __device__ __forceinline__ int layer_of(const int* pre, int L, int p) {
   return lo;
 }
 
-// Bounded wait until *flag >= target (acquire); on timeout: error word + counter.
-__device__ void wait_flag(const uint32_t* flag, uint32_t target, const DevState& s) {
+// Bounded wait until *flag >= target (acquire); on timeout: error word + counter.  The
+// poll interval doubles from 32 ns up to max_sleep_ns.
+__device__ void wait_flag(const uint32_t* flag, uint32_t target, const DevState& s, unsigned max_sleep_ns = 2048) {
   if (ld_acquire_u32(flag) >= target) return;
   const uint64_t t0 = global_timer_ns();
   unsigned ns = 32;
@@ -70,7 +71,7 @@ __device__ void wait_flag(const uint32_t* flag, uint32_t target, const DevState&
       return;
     }
     __nanosleep(ns);
-    if (ns < 2048) ns <<= 1;
+    if (ns < max_sleep_ns) ns <<= 1;
   }
 }
 
@@ -83,9 +84,9 @@ struct AttSmem {
 };
 
 struct SelSmem {
-  uint16_t scores[kSelChunk];  // scores of the chunk's tokens
-  uint32_t hist[kNBPad];       // histogram of the chunk's scores
-  uint32_t tot[kNBPad];        // the unit's histogram (last chunk to arrive)
+  uint16_t scores[kSelChunk];       // scores of the chunk's tokens
+  uint32_t hist[kCompWarps][kNBPad]; // histogram of each warp's segment of the chunk
+  uint32_t tot[kNBPad];             // the unit's histogram (last chunk to arrive)
   int wc[kCompWarps][2];
   int misc[8];
 };
@@ -96,28 +97,96 @@ union CompSmem {
   SelSmem sel;
 };
 
+// ---- hash-code scores -------------------------------------------------------------------
+// score(k) = sum_g (128 - popc(k ^ q_g)) over the G query codes of the group.  Per bit j let
+// c_j = number of query codes with bit j set; then the summed Hamming distance is
+//   X(k) = sum_j (k_j ? G - c_j : c_j),
+// a sum of small numbers v_j.  With the binary digits of c_j and of G - c_j held as bit
+// planes A_p and B_p (p < NP), digit p of v_j is one bit-select, (k & B_p) | (~k & A_p),
+// and X = sum_p 2^p popc(V_p).  A carry-save adder tree folds the NP x 4 plane words into
+// one word per weight, so a token costs 5 or 6 popcounts instead of 4 G.
 template <int G>
-__device__ __forceinline__ int score_of(const uint4 c, const uint64_t* qw) {
-  const uint64_t k0 = (uint64_t)c.x | ((uint64_t)c.y << 32);
-  const uint64_t k1 = (uint64_t)c.z | ((uint64_t)c.w << 32);
-  int sc = 128 * G;
-#pragma unroll
-  for (int g = 0; g < G; ++g) sc -= __popcll(k0 ^ qw[2 * g]) + __popcll(k1 ^ qw[2 * g + 1]);
-  return sc;
-}
+struct QPlanes {
+  static constexpr int NP = G < 2 ? 1 : (G < 4 ? 2 : (G < 8 ? 3 : 4));  // digits of 0..G
+  uint32_t A[NP][4], B[NP][4];
+};
 
 template <int G>
-__device__ __forceinline__ void load_qcodes(const DevState& s, int64_t u, uint64_t* qw) {
+__device__ __forceinline__ void load_qplanes(const DevState& s, int64_t u, QPlanes<G>& qp) {
+  constexpr int NP = QPlanes<G>::NP;
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
   const int l = (int)(u / ((int64_t)s.Hkv * s.B));
   const uint4* qc = s.qcodes + ((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G;
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 v = qc[g];
-    qw[2 * g] = (uint64_t)v.x | ((uint64_t)v.y << 32);
-    qw[2 * g + 1] = (uint64_t)v.z | ((uint64_t)v.w << 32);
+  for (int w = 0; w < 4; ++w) {
+    uint32_t cnt[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) cnt[p] = 0u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {  // bit-sliced counter += query word
+      const uint4 v = qc[g];
+      uint32_t carry = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const uint32_t t = cnt[p] & carry;
+        cnt[p] ^= carry;
+        carry = t;
+      }
+    }
+    // G - c = (~c) + (G + 1) mod 2^NP, bit-sliced with the constant's digits
+    uint32_t carry = 0u;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const uint32_t x = ~cnt[p];
+      const uint32_t gb = ((G + 1) >> p) & 1 ? 0xffffffffu : 0u;
+      qp.A[p][w] = cnt[p];
+      qp.B[p][w] = x ^ gb ^ carry;
+      carry = (x & gb) | (x & carry) | (gb & carry);
+    }
   }
+}
+
+__device__ __forceinline__ void csa(uint32_t& sum, uint32_t& carry, uint32_t a, uint32_t b, uint32_t c) {
+  sum = a ^ b ^ c;
+  carry = (a & b) | (a & c) | (b & c);
+}
+
+template <int G>
+__device__ __forceinline__ int score_of(const uint4 c, const QPlanes<G>& qp) {
+  constexpr int NP = QPlanes<G>::NP;
+  const uint32_t k[4] = {c.x, c.y, c.z, c.w};
+  uint32_t v[4][4];  // digit planes of v_j (absent planes are zero and fold away)
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) v[p][w] = p < NP ? ((k[w] & qp.B[p < NP ? p : 0][w]) | (~k[w] & qp.A[p < NP ? p : 0][w])) : 0u;
+  // weight 1: 4 words -> o1 + 2 carries of weight 2
+  uint32_t s, o1, k1, k2;
+  csa(s, k1, v[0][0], v[0][1], v[0][2]);
+  o1 = s ^ v[0][3];
+  k2 = s & v[0][3];
+  // weight 2: 4 words + 2 carries -> o2 + 3 carries of weight 4
+  uint32_t s1, s2, o2, m1, m2, m3;
+  csa(s1, m1, v[1][0], v[1][1], v[1][2]);
+  csa(s2, m2, v[1][3], k1, k2);
+  o2 = s1 ^ s2;
+  m3 = s1 & s2;
+  // weight 4: 4 words + 3 carries -> o4 + 3 carries of weight 8
+  uint32_t t1, t2, o4, n1, n2, n3;
+  csa(t1, n1, v[2][0], v[2][1], v[2][2]);
+  csa(t2, n2, v[2][3], m1, m2);
+  csa(o4, n3, t1, t2, m3);
+  // weight 8: 4 words + 3 carries -> o8 + 3 carries of weight 16
+  uint32_t r1, r2, o8, p1, p2, p3;
+  csa(r1, p1, v[3][0], v[3][1], v[3][2]);
+  csa(r2, p2, v[3][3], n1, n2);
+  csa(o8, p3, r1, r2, n3);
+  // weight 16: 3 words -> o16 + a carry of weight 32
+  uint32_t o16, o32;
+  csa(o16, o32, p1, p2, p3);
+  const int X = __popc(o1) + 2 * __popc(o2) + 4 * __popc(o4) + 8 * __popc(o8) + 16 * __popc(o16) + 32 * __popc(o32);
+  return 128 * G - X;
 }
 
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
@@ -128,21 +197,24 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
 
 // ---- selection item: one chunk of kSelChunk tokens of one unit --------------------------
 // Scores are small integers (0 .. 128 G), so the top-k is one histogram digit:
-//   1. score the chunk's tokens (16-byte codes read once, coalesced), keep the scores in
-//      shared memory, build the chunk's histogram and add it into the unit's histogram;
+//   1. each warp scores its contiguous quarter of the chunk (16-byte codes read once,
+//      coalesced), keeps the scores in shared memory and builds its own histogram; the
+//      chunk's histogram is added into the unit's histogram in global memory;
 //   2. the chunk that arrives last finds the unit's threshold T, the largest score with
 //      count(score >= T) >= k, and publishes T and n_gt = count(score > T);
 //   3. each chunk publishes its counts above and at T; from the counts of the chunks
 //      before it, a chunk knows where its indices go and how many of its ties it takes
 //      (ties go to the lowest token index: the quota k - n_gt is filled in chunk order);
-//   4. ordered compaction of the chunk from the scores in shared memory.
+//   4. ordered compaction of each warp's quarter from the scores in shared memory.
 // The chunks of a unit sit next to each other in the work queue and every group runs its
 // item to the end, so the waits of steps 2 and 3 only target items already running
 // (provided at least nch groups run; the host checks this).
 template <int G>
 __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int gtid) {
   constexpr int NB = 128 * G + 1;
-  constexpr int kU = 8;  // code loads in flight per thread
+  constexpr int kU = 8;                          // code loads in flight per lane
+  constexpr int WSEG = kSelChunk / kCompWarps;   // tokens per warp
+  static_assert(WSEG % (32 * kU) == 0, "warp segment is whole rounds");
   const int NC = s.nch;
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
@@ -150,34 +222,39 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   const int64_t t0 = (int64_t)c * kSelChunk;
   const int len = (int)(N - t0 <= 0 ? 0 : (N - t0 < kSelChunk ? N - t0 : kSelChunk));
   const int warp = gtid >> 5, lane = gtid & 31;
-  for (int i = gtid; i < NB; i += kCompThreads) sm.hist[i] = 0;
-  uint64_t qw[2 * G];
-  load_qcodes<G>(s, u, qw);
-  comp_bar();
+  uint32_t* wh = sm.hist[warp];
+  for (int i = lane; i < NB; i += 32) wh[i] = 0;
+  QPlanes<G> qp;
+  load_qplanes<G>(s, u, qp);
+  __syncwarp();
 
-  // 1. scores and histograms
+  // 1. scores and histograms of this warp's segment [w0, w1)
+  const int w0 = warp * WSEG;
+  const int w1 = (w0 + WSEG < len) ? w0 + WSEG : len;
   const uint4* src = s.codes + u * s.Nmax + t0;
-  for (int base = 0; base < len; base += kCompThreads * kU) {
+  for (int base = w0; base < w1; base += 32 * kU) {
     uint4 cv[kU];
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
-      const int t = base + kCompThreads * j + gtid;
-      if (t < len) cv[j] = ld_nc_v4(src + t);
+      const int t = base + 32 * j + lane;
+      if (t < w1) cv[j] = ld_nc_v4(src + t);
     }
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
-      const int t = base + kCompThreads * j + gtid;
-      if (t < len) {
-        const int sc = score_of<G>(cv[j], qw);
+      const int t = base + 32 * j + lane;
+      if (t < w1) {
+        const int sc = score_of<G>(cv[j], qp);
         sm.scores[t] = (uint16_t)sc;
-        atomicAdd(&sm.hist[sc], 1u);
+        atomicAdd(&wh[sc], 1u);
       }
     }
   }
   comp_bar();
   uint32_t* UH = s.unit_hist + u * s.nbp;
   for (int i = gtid; i < NB; i += kCompThreads) {
-    const uint32_t v = sm.hist[i];
+    uint32_t v = 0;
+#pragma unroll
+    for (int w = 0; w < kCompWarps; ++w) v += sm.hist[w][i];
     if (v) atomicAdd(UH + i, v);
   }
   __threadfence();
@@ -218,7 +295,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     }
   }
   if (gtid == 0) {
-    wait_flag(&s.fin_done[u], 1u, s);
+    wait_flag(&s.fin_done[u], 1u, s, 256);
     const int2 th = __ldcg(&s.sel_thr[u]);
     sm.misc[1] = th.x < 0 ? 0 : (th.x >= NB ? NB - 1 : th.x);  // clamped: garbage only after a timeout
     sm.misc[2] = th.y;
@@ -227,17 +304,30 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   const int T = sm.misc[1], n_gt = sm.misc[2];
   const int quota = k - n_gt;  // ties to take, unit-wide, lowest index first
 
-  // 3. this chunk's counts; offsets from the chunks before it
-  if (warp == 0) {
+  // 3. counts of each warp's segment; the chunk's counts; offsets from earlier chunks
+  {
     int gt = 0;
-    for (int bin = T + 1 + lane; bin < NB; bin += 32) gt += (int)sm.hist[bin];
+    for (int bin = T + 1 + lane; bin < NB; bin += 32) gt += (int)wh[bin];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
     if (lane == 0) {
-      s.sel_meta[u * NC + c] = make_int2(gt, (int)sm.hist[T]);
+      sm.wc[warp][0] = gt;
+      sm.wc[warp][1] = (int)wh[T];
+    }
+  }
+  comp_bar();
+  int eq_c = 0;
+#pragma unroll
+  for (int w = 0; w < kCompWarps; ++w) eq_c += sm.wc[w][1];
+  if (warp == 0) {
+    if (lane == 0) {
+      int gt_c = 0;
+#pragma unroll
+      for (int w = 0; w < kCompWarps; ++w) gt_c += sm.wc[w][0];
+      s.sel_meta[u * NC + c] = make_int2(gt_c, eq_c);
       __threadfence();
       red_release_add_u32(&s.cnt_done[u], 1u);
-      wait_flag(&s.cnt_done[u], (uint32_t)NC, s);
+      wait_flag(&s.cnt_done[u], (uint32_t)NC, s, 256);
     }
     __syncwarp();
     int base_sel = 0, eq_before = 0;
@@ -263,33 +353,11 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     }
   }
   comp_bar();
-  const int out_base = sm.misc[3];
-  int take_eq = quota - sm.misc[4];
-  take_eq = take_eq < 0 ? 0 : (take_eq > (int)sm.hist[T] ? (int)sm.hist[T] : take_eq);
+  int take_eq = quota - sm.misc[4];  // ties this chunk takes
+  take_eq = take_eq < 0 ? 0 : (take_eq > eq_c ? eq_c : take_eq);
 
-  // 4. ordered compaction: warp w owns tokens [w * seg, (w + 1) * seg) of the chunk
-  const int wseg = ((len + kCompWarps - 1) / kCompWarps + 31) / 32 * 32;
-  const int w0 = warp * wseg;
-  const int w1 = (w0 + wseg < len) ? w0 + wseg : len;
-  {
-    int gt = 0, eq = 0;
-    for (int t = w0 + lane; t < w1; t += 32) {
-      const int sc = sm.scores[t];
-      gt += sc > T;
-      eq += sc == T;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o);
-      eq += __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if (lane == 0) {
-      sm.wc[warp][0] = gt;
-      sm.wc[warp][1] = eq;
-    }
-  }
-  comp_bar();
-  int off = out_base, eqb = 0;
+  // 4. ordered compaction of this warp's segment
+  int off = sm.misc[3], eqb = 0;
   for (int w = 0; w < warp; ++w) {
     int tk = take_eq - eqb;
     tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);

@@ -38,8 +38,9 @@ def test_warmup_profiling_and_persistent_heads():
     assert sum(r["hit"] for r in log[4:]) > 0
 
 
-def test_ragged_sequences_and_cluster_selection():
-    # three sequences of different lengths; the longest spans a 4-CTA cluster; G = 5
+def test_ragged_sequences_and_multi_chunk_selection():
+    # three sequences of different lengths: 5, 3 and 1 selection chunks of 8192 tokens,
+    # ragged last chunks, empty chunks for the shorter sequences; G = 5
     spec = Spec(L=1, B=3, Hq=10, Hkv=2, d=128, ntok=[40000, 17000, 3001], seed=7, tau=0.8, rho=(0.7, 0.98))
     _run(spec, 4)
 
@@ -60,13 +61,15 @@ def test_single_token_context():
     _run(spec, 3)
 
 
-def test_all_scores_tied_selects_lowest_indices():
-    # all-zero keys: every key code is 0 and every score ties -> selection {0..k-1}
-    L, B, Hkv, d, N = 1, 1, 2, 64, 5000
+@pytest.mark.parametrize("N,topk", [(5000, 0), (20000, 10000)])
+def test_all_scores_tied_selects_lowest_indices(N, topk):
+    # all-zero keys: every key code is 0 and every score ties -> selection {0..k-1}; with
+    # N = 20000 and k = 10000 the tie quota fills chunk 0 and part of chunk 1
+    L, B, Hkv, d = 1, 1, 2, 64
     K = np.zeros((N, Hkv, d), dtype=np.uint16)
     V = np.zeros((N, Hkv, d), dtype=np.uint16)
     V[:, :, :] = np.arange(N, dtype=np.uint16)[:, None, None] & 0x3fff   # distinct finite values
-    spec = Spec(L=L, B=B, Hq=4, Hkv=Hkv, d=d, ntok=[N], seed=13, tau=2.0, kv_override={(0, 0): (K, V)})
+    spec = Spec(L=L, B=B, Hq=4, Hkv=Hkv, d=d, ntok=[N], seed=13, tau=2.0, topk=topk, kv_override={(0, 0): (K, V)})
     ls = LockStep(spec)
     try:
         ls.check_key_codes()
