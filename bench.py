@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0,
                    help="override the batch (for workloads whose host pool exceeds the box's memory)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layerwise", action="store_true",
+                   help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-steps", type=int, default=2, help="oracle steps timed for the CPU baseline")
     return p.parse_args()
@@ -226,6 +228,13 @@ def run_gb300(args, rank, world, local_rank):
                      topk=w.topk, topk_ratio=w.topk_ratio, tau=tau, warmup_steps=w.warmup_steps,
                      tau_offset=w.tau_offset, n_persist=w.n_persist if tau is None else 0, timing=True,
                      stream=stream.cuda_stream)
+    if args.layerwise:
+        def step_fn(q, o, io_on_device=None):
+            for l in range(L):
+                lib.decode_layer(l, q[l], o[l], io_on_device)
+    else:
+        def step_fn(q, o, io_on_device=None):
+            lib.decode_step(q, o, io_on_device)
     Kbuf = np.empty((N, Hkv, d), dtype=np.uint16)
     Vbuf = np.empty((N, Hkv, d), dtype=np.uint16)
     for l in range(L):
@@ -248,7 +257,7 @@ def run_gb300(args, rank, world, local_rank):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(n_prof + W):
-            lib.decode_step(qdev[i], out)
+            step_fn(qdev[i], out)
     lib.sync()
     lib.stats()  # drops the per-phase events of untimed steps
     before = lib.stats()
@@ -264,7 +273,7 @@ def run_gb300(args, rank, world, local_rank):
     ev0.record(stream)
     with torch.cuda.stream(stream):
         for i in range(K):
-            lib.decode_step(qdev[n_prof + W + i], out)
+            step_fn(qdev[n_prof + W + i], out)
     ev1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -293,13 +302,13 @@ def run_gb300(args, rank, world, local_rank):
             qs.next(qh)
             qpin[i].copy_(torch.from_numpy(qh.view(np.int16)))
         opin = torch.empty((L, B, Hq, d), dtype=torch.float32, pin_memory=True)
-        lib.decode_step(qpin[0].numpy(), opin.numpy(), io_on_device=False)
+        step_fn(qpin[0].numpy(), opin.numpy(), io_on_device=False)
         lib.stats()
         if world > 1:
             torch.distributed.barrier()
         t1 = time.perf_counter()
         for i in range(1, Ke):
-            lib.decode_step(qpin[i].numpy(), opin.numpy(), io_on_device=False)
+            step_fn(qpin[i].numpy(), opin.numpy(), io_on_device=False)
         t2 = time.perf_counter()
         lib.stats()
         sec = max_over_ranks(t2 - t1, world)
@@ -349,8 +358,9 @@ def run_gb300(args, rank, world, local_rank):
                    else w.tau_fixed, "kv_dtype": "bf16", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
-                   "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1)},
-        "gpu_launches": 3 * steps,
+                   "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1),
+                   "mode": "layer by layer (clo_decode_layer per layer)" if args.layerwise else "whole step"},
+        "gpu_launches": 2 * steps * (L if args.layerwise else 1),
         "roofline": roofline,
         "step_roofline": {"bound": "max(HBM alg bytes / HBM peak, host bytes / link peak)",
                           "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,

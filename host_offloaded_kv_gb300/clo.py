@@ -24,8 +24,8 @@ CLO_SET_DROP_FLAG_LAYER, CLO_SET_WAIT_TIMEOUT_NS = 1, 2
 _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ERR_CUDA", 4: "CLO_ERR_TIMEOUT",
                  5: "CLO_ERR_STATE", 6: "CLO_ERR_CAPACITY", 7: "CLO_ERR_DEVICE"}
 
-EXPORTED = ["clo_config_default", "clo_init", "clo_destroy", "clo_append_kv", "clo_decode_step", "clo_sync",
-            "clo_stats", "clo_last_error", "clo_debug_get", "clo_set", "clo_sparse_attention_noalloc"]
+EXPORTED = ["clo_config_default", "clo_init", "clo_destroy", "clo_append_kv", "clo_decode_step", "clo_decode_layer",
+            "clo_sync", "clo_stats", "clo_last_error", "clo_debug_get", "clo_set", "clo_sparse_attention_noalloc"]
 
 
 class CLOError(RuntimeError):
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH):
     lib.clo_append_kv.argtypes = [vp, i32, i32, vp, vp, i64, i32]
     lib.clo_decode_step.restype = ctypes.c_int
     lib.clo_decode_step.argtypes = [vp, vp, vp, i32]
+    lib.clo_decode_layer.restype = ctypes.c_int
+    lib.clo_decode_layer.argtypes = [vp, i32, vp, vp, i32]
     lib.clo_sync.restype = ctypes.c_int
     lib.clo_sync.argtypes = [vp]
     lib.clo_stats.restype = ctypes.c_int
@@ -160,6 +162,13 @@ def clo_decode_step(ctx, q, out, io_on_device: bool | None = None) -> None:
     op, odev = _ptr(out)
     dev = qdev if io_on_device is None else bool(io_on_device)
     _check(load_library().clo_decode_step(ctx, qp, op, int(bool(dev))), "clo_decode_step")
+
+
+def clo_decode_layer(ctx, layer: int, q, out, io_on_device: bool | None = None) -> None:
+    qp, qdev = _ptr(q)
+    op, odev = _ptr(out)
+    dev = qdev if io_on_device is None else bool(io_on_device)
+    _check(load_library().clo_decode_layer(ctx, int(layer), qp, op, int(bool(dev))), "clo_decode_layer")
 
 
 def clo_sync(ctx) -> None:
@@ -251,6 +260,10 @@ class CLOContext:
     def decode_step(self, q, out, io_on_device=None):
         clo_decode_step(self.ctx, q, out, io_on_device)
 
+    def decode_layer(self, layer, q, out, io_on_device=None):
+        """One layer of a step: q bf16 [B][Hq][d], out fp32 [B][Hq][d]; layers in order."""
+        clo_decode_layer(self.ctx, layer, q, out, io_on_device)
+
     def sync(self):
         clo_sync(self.ctx)
 
@@ -304,4 +317,4 @@ class CLOContext:
                 "selection_chunk_mean_us": round(int(t[9]) / 1e3 / max(1, int(t[10])), 2),
                 "selection_chunks": int(t[10]),
                 "attention_split_mean_us": round(int(t[11]) / 1e3 / max(1, int(t[12])), 2),
-                "attention_splits": int(t[12])}
+                "attention_splits": int(t[12]), "decide_start_us": rel(t[13]), "decide_end_us": rel(t[14])}

@@ -59,6 +59,7 @@ struct clo_ctx {
   int64_t* ntok_pinned = nullptr;  // [B] + k [B] staging for uploads
   int64_t step = 0;
   bool warmup_mode = false;
+  int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
   int W = 0;
   bool warmup_done = false;
   uint16_t* kstage = nullptr;
@@ -231,7 +232,10 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   }
   // per-step zeroed region: step counters, per-layer list lengths, work queues, ready
   // flags of the fetch chunks, selection progress counters
-  s.nch = (int)((c->Nmax + kSelChunk - 1) / kSelChunk);
+  // selection chunks: 8192 tokens up to 32K contexts (enough chunks per unit to select a
+  // unit quickly), 16384 beyond (fewer threshold hand-offs per token)
+  s.sel_chunk = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
+  s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
   s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
   {
     size_t off = 2 * (size_t)C_NUM * kCtrLanes;
@@ -243,8 +247,6 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     off += (size_t)U * s.nchunk;
     const size_t o_sel = off;
     off += 4 * (size_t)U;
-    const size_t o_hist = off;
-    off += (size_t)U * s.nbp;
     off = (off + 1) / 2 * 2;  // 8-byte alignment for the timeline
     const size_t o_tl = off;
     off += 2 * (size_t)kTimelineSlots;
@@ -260,13 +262,13 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.fin_done = z + o_sel + U;
     s.cnt_done = z + o_sel + 2 * U;
     s.sel_cnt = z + o_sel + 3 * U;
-    s.unit_hist = z + o_hist;
     c->timeline_dev = reinterpret_cast<unsigned long long*>(z + o_tl);
     s.timeline = cfg->timing ? c->timeline_dev : nullptr;
   }
   CLO_TRY(c->dalloc(&s.hit_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.pers_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.miss_list, (size_t)c->L * c->B * c->Hkv));
+  CLO_TRY(c->dalloc(&s.unit_hist, (size_t)U * s.nbp));
   CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * s.nch));
   CLO_TRY(c->dalloc(&s.sel_thr, (size_t)U));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
@@ -344,6 +346,7 @@ CLO_API clo_status clo_append_kv(clo_ctx* c, int32_t layer, int32_t seq, const v
   if (!c) return fail(CLO_ERR_INVALID, "null context");
   if (layer < 0 || layer >= c->L || seq < 0 || seq >= c->B) return fail(CLO_ERR_INVALID, "layer/seq out of range");
   if (n_tokens < 0 || (n_tokens > 0 && (!k || !v))) return fail(CLO_ERR_INVALID, "bad k/v/n_tokens");
+  if (c->next_layer != 0) return fail(CLO_ERR_STATE, "a layer-by-layer step is in progress");
   int64_t& cur = c->ntok[(size_t)layer * c->B + seq];
   if (cur + n_tokens > c->Nmax)
     return fail(CLO_ERR_CAPACITY, "append of " + std::to_string(n_tokens) + " tokens exceeds max_tokens " +
@@ -391,23 +394,12 @@ static clo_status refresh_lengths(clo_ctx* c) {
   return CLO_OK;
 }
 
-CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_t io_on_device) {
-  if (!c) return fail(CLO_ERR_INVALID, "null context");
-  if (!q || !out) return fail(CLO_ERR_INVALID, "null q/out");
-  if (c->ntok_dirty) CLO_TRY(refresh_lengths(c));
-  const size_t nq = (size_t)c->L * c->B * c->Hq * c->d;
-  const uint16_t* qd = static_cast<const uint16_t*>(q);
-  float* od = out;
-  if (!io_on_device) {
-    if (!c->q_io) {
-      CLO_TRY(c->dalloc(&c->q_io, nq));
-      CLO_TRY(c->dalloc(&c->out_io, nq));
-    }
-    CLO_CUDA(cudaMemcpyAsync(c->q_io, q, sizeof(uint16_t) * nq, cudaMemcpyHostToDevice, c->stream));
-    qd = c->q_io;
-    od = c->out_io;
-  }
+// Enqueues layers [l0, l1) of the current step: q / out hold those layers' blocks.
+static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd, float* od) {
   DevState& s = c->ds;
+  s.l0 = l0;
+  s.l1 = l1;
+  s.q_l0 = l0;
   const bool warm = c->warmup_mode && c->step < c->W;
   const bool timed = c->cfg.timing != 0;
   cudaEvent_t* ev = nullptr;
@@ -419,20 +411,79 @@ CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_
     }
     ev = c->ev_pool[c->ev_used++].data();
   }
-  ++c->epoch;
+  if (l0 == 0) ++c->epoch;
   if (timed) CLO_CUDA(cudaEventRecord(ev[0], c->stream));
-  CLO_CUDA(cudaMemsetAsync(c->step_zero, 0, c->step_zero_bytes, c->stream));
+  // the step's counters are zeroed once per step; queues, lists and flags per launch
+  const size_t ctr_bytes = l0 == 0 ? 0 : sizeof(unsigned long long) * C_NUM * kCtrLanes;
+  CLO_CUDA(cudaMemsetAsync(reinterpret_cast<unsigned char*>(c->step_zero) + ctr_bytes, 0,
+                           c->step_zero_bytes - ctr_bytes, c->stream));
   CLO_CUDA(launch_decide(s, qd, c->step, warm ? 1 : 0, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[1], c->stream));
   CLO_CUDA(launch_step_fused(s, qd, od, c->stream));
   if (timed) CLO_CUDA(cudaEventRecord(ev[2], c->stream));
-  if (warm && c->step == c->W - 1) {
-    CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
-    CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
-    c->warmup_done = true;
-    c->persist_host_valid = false;
+  if (l1 == c->L) {  // the step is complete
+    if (warm && c->step == c->W - 1) {
+      CLO_CUDA(launch_finish_warmup(s, c->W, c->cfg.tau_offset, c->cfg.n_persist, c->stream));
+      CLO_CUDA(launch_resident_fill(s, 0, c->Nmax, c->stream));
+      c->warmup_done = true;
+      c->persist_host_valid = false;
+    }
+    ++c->step;
   }
-  ++c->step;
+  c->next_layer = l1 == c->L ? 0 : l1;
+  return CLO_OK;
+}
+
+// Host-buffer mode: stage nq elements of q into the device copy; returns the device
+// pointers to use.
+static clo_status stage_io(clo_ctx* c, const void* q, float* out, size_t nq, int32_t io_on_device,
+                           const uint16_t** qd, float** od) {
+  *qd = static_cast<const uint16_t*>(q);
+  *od = out;
+  if (io_on_device) return CLO_OK;
+  if (!c->q_io) {
+    const size_t full = (size_t)c->L * c->B * c->Hq * c->d;
+    CLO_TRY(c->dalloc(&c->q_io, full));
+    CLO_TRY(c->dalloc(&c->out_io, full));
+  }
+  CLO_CUDA(cudaMemcpyAsync(c->q_io, q, sizeof(uint16_t) * nq, cudaMemcpyHostToDevice, c->stream));
+  *qd = c->q_io;
+  *od = c->out_io;
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_decode_step(clo_ctx* c, const void* q, float* out, int32_t io_on_device) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  if (!q || !out) return fail(CLO_ERR_INVALID, "null q/out");
+  if (c->next_layer != 0)
+    return fail(CLO_ERR_STATE, "a layer-by-layer step is in progress (next layer " +
+                                   std::to_string(c->next_layer) + ")");
+  if (c->ntok_dirty) CLO_TRY(refresh_lengths(c));
+  const size_t nq = (size_t)c->L * c->B * c->Hq * c->d;
+  const uint16_t* qd = nullptr;
+  float* od = nullptr;
+  CLO_TRY(stage_io(c, q, out, nq, io_on_device, &qd, &od));
+  CLO_TRY(enqueue_layers(c, 0, c->L, qd, od));
+  if (!io_on_device) {
+    CLO_CUDA(cudaMemcpyAsync(out, c->out_io, sizeof(float) * nq, cudaMemcpyDeviceToHost, c->stream));
+    return clo_sync(c);
+  }
+  return CLO_OK;
+}
+
+CLO_API clo_status clo_decode_layer(clo_ctx* c, int32_t layer, const void* q, float* out, int32_t io_on_device) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  if (!q || !out) return fail(CLO_ERR_INVALID, "null q/out");
+  if (layer < 0 || layer >= c->L) return fail(CLO_ERR_INVALID, "layer out of range");
+  if (layer != c->next_layer)
+    return fail(CLO_ERR_STATE, "layers must be decoded in order: expected layer " + std::to_string(c->next_layer) +
+                                   ", got " + std::to_string(layer));
+  if (layer == 0 && c->ntok_dirty) CLO_TRY(refresh_lengths(c));
+  const size_t nq = (size_t)c->B * c->Hq * c->d;
+  const uint16_t* qd = nullptr;
+  float* od = nullptr;
+  CLO_TRY(stage_io(c, q, out, nq, io_on_device, &qd, &od));
+  CLO_TRY(enqueue_layers(c, layer, layer + 1, qd, od));
   if (!io_on_device) {
     CLO_CUDA(cudaMemcpyAsync(out, c->out_io, sizeof(float) * nq, cudaMemcpyDeviceToHost, c->stream));
     return clo_sync(c);

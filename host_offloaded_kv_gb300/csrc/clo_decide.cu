@@ -1,4 +1,4 @@
-// Head-wise reuse decision and query hashing (one CTA per unit).
+// Head-wise reuse decision and query hashing (one CTA per kv head and group of sequences).
 //
 // Reuse test: adjacent-step query cosine similarity is high (> 0.8) on most
 // heads, which CLO turns into a cache-reuse condition ("CLO (2511.14510) - L3
@@ -16,8 +16,9 @@ namespace clo {
 
 namespace {
 
-constexpr int kDecideThreads = 512;  // one thread per (query head, code bit) for G <= 4
-constexpr int kDecideWarps = kDecideThreads / 32;
+constexpr int kDecideThreads = 512;
+constexpr int kHashSlots = kDecideThreads / 128;  // threads per code bit
+constexpr int kMaxRows = 32;                        // hashed query rows per CTA
 
 struct StridedF32 {
   const float* p;
@@ -30,140 +31,189 @@ struct StridedBF16 {
   __device__ float operator()(int i) const { return bf16_bits_to_f32(p[i * stride]); }
 };
 
-// One CTA per unit.  The head's projection R (d x 128 bf16) is staged in shared
-// memory by asynchronous 16-byte copies that overlap the reuse test; each thread
-// then hashes one (query head, code bit) pair.
+// Units of one kv head handled by one CTA: as many sequences as fit 32 query rows,
+// at most one per warp.
+__host__ __device__ inline int units_per_cta(int G, int B) {
+  int n = kMaxRows / G;
+  n = n < 1 ? 1 : (n > kDecideThreads / 32 ? kDecideThreads / 32 : n);
+  return n < B ? n : B;
+}
+
+// One CTA per (layer, kv head, group of up to 32 / G sequences).  The head's
+// projection R (d x 128 bf16) is staged once in shared memory by asynchronous
+// 16-byte copies that overlap the reuse tests.  Warp w decides unit w from the query
+// it holds in registers and writes the unit's G query rows (rows w*G .. w*G+G-1) to
+// a transposed fp32 copy [d][slot][M] (row r at column (r % slots) * M + r / slots);
+// then thread (slot, bit j) computes bit j of M rows at once from broadcast float4
+// loads.
+//   dynamic shared memory: Rs bf16 [d][128] | xs fp32 [d][kHashSlots * M]
+template <int M>
 __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uint16_t* __restrict__ q, int64_t step,
                                                             int warmup_active) {
-  __shared__ __align__(16) uint16_t Rs[kMaxD * 128];
-  __shared__ float qs[kMaxG * kMaxD];
-  __shared__ float red[3][kDecideWarps];
-  __shared__ int s_dec;
-  __shared__ uint32_t words[kMaxG][4];
-  __shared__ unsigned char s_valid, s_persist;
-  __shared__ float s_tau;
-  __shared__ long long s_N, s_k;
+  extern __shared__ __align__(16) unsigned char dsm[];
+  constexpr int XW = kHashSlots * M;  // floats per dimension in xs
+  __shared__ int s_dec[kMaxRows];
+  __shared__ uint32_t words[kMaxRows][4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t u = blockIdx.x;
-  const int h = (int)(u % s.Hkv);
-  const int b = (int)((u / s.Hkv) % s.B);
-  const int l = (int)(u / ((int64_t)s.Hkv * s.B));
-  const int lh = l * s.Hkv + h;
   const int G = s.G, d = s.d, GD = s.G * s.d;
+  const int UPC = units_per_cta(G, s.B);
+  const int ngrp = (s.B + UPC - 1) / UPC;
+  const int lh = s.l0 * s.Hkv + (int)(blockIdx.x / ngrp);
+  const int b0 = (blockIdx.x % ngrp) * UPC;
+  const int nu = (s.B - b0) < UPC ? (s.B - b0) : UPC;
+  const int l = lh / s.Hkv, h = lh % s.Hkv;
+  uint16_t* Rs = reinterpret_cast<uint16_t*>(dsm);
+  float* xs = reinterpret_cast<float*>(dsm + (size_t)d * 128 * 2);
+  if (tid == 0 && s.timeline) atomicCAS(&s.timeline[TL_DEC_START], 0ull, global_timer_ns());
   {
     const uint4* src = reinterpret_cast<const uint4*>(s.R + (int64_t)lh * d * 128);
     for (int e = tid; e < d * 128 / 8; e += kDecideThreads) cp_async16(&Rs[e * 8], src + e);
     cp_async_commit();
   }
-  // the unit's scalars, loaded in parallel by different warps
-  if (tid == 32) s_valid = s.qvalid[u];
-  if (tid == 64) s_persist = s.persist[lh];
-  if (tid == 96) s_tau = s.tau[lh];
-  if (tid == 128) s_N = s.ntok[b];
-  if (tid == 160) s_k = s.kcount[b];
 
-  const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * d;
-  uint16_t* qc = s.qcache + u * GD;
-  float dot = 0.f, nq = 0.f, nc = 0.f;
-  for (int e = tid; e < GD; e += kDecideThreads) {
-    const float x = bf16_bits_to_f32(qg[e]);
-    const float c = bf16_bits_to_f32(qc[e]);
-    qs[e] = x;
-    dot = fmaf(x, c, dot);
-    nq = fmaf(x, x, nq);
-    nc = fmaf(c, c, nc);
-  }
-  dot = warp_sum(dot);
-  nq = warp_sum(nq);
-  nc = warp_sum(nc);
-  if (lane == 0) {
-    red[0][warp] = dot;
-    red[1][warp] = nq;
-    red[2][warp] = nc;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float D = 0.f, Q = 0.f, C = 0.f;
-    for (int w = 0; w < kDecideWarps; ++w) {
-      D += red[0][w];
-      Q += red[1][w];
-      C += red[2][w];
+  // 1. reuse test of unit w by warp w; its query rows go to xs from registers
+  if (warp < nu) {
+    const int b = b0 + warp;
+    const int64_t u = ((int64_t)l * s.B + b) * s.Hkv + h;
+    // the unit's scalars, loaded up front (independent loads)
+    const bool valid = s.qvalid[u] != 0;
+    const bool pers = s.persist[lh] != 0;
+    const float tau = s.tau[lh];
+    const int64_t N = s.ntok[b], k = s.kcount[b];
+    const uint16_t* qg = q + (((int64_t)(l - s.q_l0) * s.B + b) * s.Hq + (int64_t)h * G) * d;
+    uint16_t* qc = s.qcache + u * GD;
+    constexpr int kMaxPer = kMaxG * kMaxD / 256;  // uint4 of the group's query per lane
+    uint4 xv[kMaxPer];
+    float dot = 0.f, nq = 0.f, nc = 0.f;
+#pragma unroll
+    for (int p = 0; p < kMaxPer; ++p) {
+      const int e = 8 * lane + 256 * p;
+      if (e < GD) {
+        xv[p] = *reinterpret_cast<const uint4*>(qg + e);
+        const uint4 cv = *reinterpret_cast<const uint4*>(qc + e);
+        const uint32_t xw[4] = {xv[p].x, xv[p].y, xv[p].z, xv[p].w}, cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = bf16_bits_to_f32(xw[i] & 0xffffu), x1 = bf16_bits_to_f32(xw[i] >> 16);
+          const float c0 = bf16_bits_to_f32(cw[i] & 0xffffu), c1 = bf16_bits_to_f32(cw[i] >> 16);
+          dot = fmaf(x1, c1, fmaf(x0, c0, dot));
+          nq = fmaf(x1, x1, fmaf(x0, x0, nq));
+          nc = fmaf(c1, c1, fmaf(c0, c0, nc));
+        }
+      }
     }
-    const bool valid = s_valid != 0;
-    const float cosv = (Q > 0.f && C > 0.f) ? D / (sqrtf(Q) * sqrtf(C)) : 0.f;
+    dot = warp_sum(dot);
+    nq = warp_sum(nq);
+    nc = warp_sum(nc);
+    const float cosv = (nq > 0.f && nc > 0.f) ? dot / (sqrtf(nq) * sqrtf(nc)) : 0.f;
     int dec;
-    if (warmup_active) {
+    if (warmup_active)
       dec = CLO_DEC_MISS;
-      if (step >= 1 && valid) atomicAdd(&s.shat_sum[lh], (double)cosv);
-    } else if (s_persist) {
+    else if (pers)
       dec = CLO_DEC_PERSIST;
-    } else if (!valid) {
+    else if (!valid)
       dec = CLO_DEC_MISS;
-    } else {
-      dec = (cosv >= s_tau) ? CLO_DEC_HIT : CLO_DEC_MISS;
+    else
+      dec = (cosv >= tau) ? CLO_DEC_HIT : CLO_DEC_MISS;
+    if (dec != CLO_DEC_HIT) {
+#pragma unroll
+      for (int p = 0; p < kMaxPer; ++p) {
+        const int e = 8 * lane + 256 * p;
+        if (e < GD) {
+          const uint32_t xw[4] = {xv[p].x, xv[p].y, xv[p].z, xv[p].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int ee = e + i, r = warp * G + ee / d, dim = ee % d;
+            const uint32_t bits = (i & 1) ? (xw[i >> 1] >> 16) : (xw[i >> 1] & 0xffffu);
+            xs[dim * XW + (r % kHashSlots) * M + r / kHashSlots] = bf16_bits_to_f32(bits);
+          }
+          if (dec == CLO_DEC_MISS) *reinterpret_cast<uint4*>(qc + e) = xv[p];
+        }
+      }
     }
-    s.decision[u] = (uint8_t)dec;
-    s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
-    s_dec = dec;
-  }
-  __syncthreads();
-  const int dec = s_dec;
-  if (tid == 32) {  // bookkeeping off the critical path: work lists and counters
-    const bool valid = s_valid != 0;
-    const int BH = s.B * s.Hkv;
-    const int li = dec == CLO_DEC_HIT ? 0 : (dec == CLO_DEC_PERSIST ? 1 : 2);
-    int32_t* lst = li == 0 ? s.hit_list : (li == 1 ? s.pers_list : s.miss_list);
-    lst[(int64_t)l * BH + atomicAdd(&s.lcnt[li * s.L + l], 1)] = (int32_t)u;
-    const int64_t N = s_N, k = s_k, rec = 4LL * d;
-    const unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
-    int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
-    if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
-    if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
-    if (dec == CLO_DEC_PERSIST) hbm += k * 4;
-    const int slot = dec == CLO_DEC_HIT ? C_HIT : (dec == CLO_DEC_MISS ? C_MISS : C_PERSIST);
-    atomicAdd(&s.step_ctr[ctr_at(slot, u)], 1ull);
-    atomicAdd(&s.total_ctr[ctr_at(slot, u)], 1ull);
-    if (host) {
-      atomicAdd(&s.step_ctr[ctr_at(C_HOST_BYTES, u)], host);
-      atomicAdd(&s.total_ctr[ctr_at(C_HOST_BYTES, u)], host);
+    if (lane == 0) {
+      if (warmup_active && step >= 1 && valid) atomicAdd(&s.shat_sum[lh], (double)cosv);
+      if (dec == CLO_DEC_MISS) s.qvalid[u] = 1;
+      s.decision[u] = (uint8_t)dec;
+      s.cosv[u] = valid ? cosv : __int_as_float(0x7fc00000);
+      s_dec[warp] = dec;
+      // work lists and counters
+      const int BH = s.B * s.Hkv;
+      const int li = dec == CLO_DEC_HIT ? 0 : (dec == CLO_DEC_PERSIST ? 1 : 2);
+      int32_t* lst = li == 0 ? s.hit_list : (li == 1 ? s.pers_list : s.miss_list);
+      lst[(int64_t)l * BH + atomicAdd(&s.lcnt[li * s.L + l], 1)] = (int32_t)u;
+      const int64_t rec = 4LL * d;
+      const unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
+      int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
+      if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
+      if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
+      if (dec == CLO_DEC_PERSIST) hbm += k * 4;
+      const int slot = dec == CLO_DEC_HIT ? C_HIT : (dec == CLO_DEC_MISS ? C_MISS : C_PERSIST);
+      atomicAdd(&s.step_ctr[ctr_at(slot, u)], 1ull);
+      atomicAdd(&s.total_ctr[ctr_at(slot, u)], 1ull);
+      if (host) {
+        atomicAdd(&s.step_ctr[ctr_at(C_HOST_BYTES, u)], host);
+        atomicAdd(&s.total_ctr[ctr_at(C_HOST_BYTES, u)], host);
+      }
+      atomicAdd(&s.step_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
+      atomicAdd(&s.total_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
     }
-    atomicAdd(&s.step_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
-    atomicAdd(&s.total_ctr[ctr_at(C_HBM_BYTES, u)], (unsigned long long)hbm);
-  }
-  if (dec == CLO_DEC_MISS) {
-    for (int e = tid; e < GD; e += kDecideThreads) qc[e] = qg[e];
-    if (tid == 0) s.qvalid[u] = 1;
   }
   cp_async_wait<0>();  // R staged (also before any exit: no copy may outlive the CTA)
   __syncthreads();
-  if (dec == CLO_DEC_HIT) return;  // uniform over the CTA
+  int any = 0;
+  for (int w = 0; w < nu; ++w) any |= s_dec[w] != CLO_DEC_HIT;
+  if (!any) {  // uniform over the CTA
+    if (tid == 0 && s.timeline) atomicMax(&s.timeline[TL_DEC_END], global_timer_ns());
+    return;
+  }
 
-  // query codes: thread (g, j) computes bit j of head g
-  const int j = tid & 127;
-  for (int g = tid >> 7; g < G; g += kDecideThreads / 128) {
-    const float* xg = qs + g * d;
-    float acc = 0.f, aab = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < d; ++i) {
-      const float x = xg[i];
-      const float r = bf16_bits_to_f32(Rs[i * 128 + j]);
-      acc = fmaf(x, r, acc);
-      aab = fmaf(fabsf(x), fabsf(r), aab);
+  // 2. query codes: thread (slot, j) computes bit j of rows slot, slot + 4, ... (rows of
+  //    reused units are computed but neither certified nor stored)
+  const int nrows = nu * G;
+  const int j = tid & 127, slot = tid >> 7;
+  float acc[M], aab[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) acc[m] = aab[m] = 0.f;
+  const float* xrow = xs + slot * M;
+  for (int i = 0; i < d; ++i) {
+    const float r = bf16_bits_to_f32(Rs[i * 128 + j]);
+    const float ar = fabsf(r);
+#pragma unroll
+    for (int m = 0; m < M; m += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(xrow + i * XW + m);
+      acc[m] = fmaf(x.x, r, acc[m]);
+      aab[m] = fmaf(fabsf(x.x), ar, aab[m]);
+      acc[m + 1] = fmaf(x.y, r, acc[m + 1]);
+      aab[m + 1] = fmaf(fabsf(x.y), ar, aab[m + 1]);
+      acc[m + 2] = fmaf(x.z, r, acc[m + 2]);
+      aab[m + 2] = fmaf(fabsf(x.z), ar, aab[m + 2]);
+      acc[m + 3] = fmaf(x.w, r, acc[m + 3]);
+      aab[m + 3] = fmaf(fabsf(x.w), ar, aab[m + 3]);
     }
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int row = m * kHashSlots + slot;
+    if (row >= nrows) break;                         // uniform over the warp
+    if (s_dec[row / G] == CLO_DEC_HIT) continue;     // uniform over the warp
     bool bit;
-    if (sign_certified_f32(acc, aab, d))
-      bit = acc > 0.f;
+    if (sign_certified_f32(acc[m], aab[m], d))
+      bit = acc[m] > 0.f;
     else
-      bit = hash_bit_slow(StridedF32{xg, 1}, StridedBF16{Rs + j, 128}, d);
-    const uint32_t w = __ballot_sync(0xffffffffu, bit);
-    if (lane == 0) words[g][(tid & 127) >> 5] = w;
+      bit = hash_bit_slow(StridedF32{xrow + m, XW}, StridedBF16{Rs + j, 128}, d);
+    const uint32_t wbits = __ballot_sync(0xffffffffu, bit);
+    if (lane == 0) words[row][j >> 5] = wbits;
   }
   __syncthreads();
-  if (tid < G) {
-    s.qcodes[((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G + tid] =
-        make_uint4(words[tid][0], words[tid][1], words[tid][2], words[tid][3]);
+  for (int r = tid; r < nrows; r += kDecideThreads) {
+    const int w = r / G, g = r % G;
+    if (s_dec[w] == CLO_DEC_HIT) continue;
+    s.qcodes[((int64_t)l * s.B + b0 + w) * s.Hq + (int64_t)h * G + g] =
+        make_uint4(words[r][0], words[r][1], words[r][2], words[r][3]);
   }
+  if (tid == 0 && s.timeline) atomicMax(&s.timeline[TL_DEC_END], global_timer_ns());
 }
 
 // End of warm-up: s_hat = mean adjacent-step cosine, tau = s_hat - offset, and the
@@ -196,11 +246,24 @@ __global__ void k_finish_warmup(DevState s, int W, float tau_offset, int n_persi
 
 }  // namespace
 
+template <int M>
+cudaError_t launch_decide_m(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st) {
+  const int upc = units_per_cta(s.G, s.B);
+  const unsigned grid = (unsigned)((s.l1 - s.l0) * s.Hkv * ((s.B + upc - 1) / upc));
+  const size_t smem = (size_t)s.d * 128 * 2 + (size_t)s.d * kHashSlots * M * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_decide<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_decide<M><<<grid, kDecideThreads, smem, st>>>(s, q, step, warmup_active);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active,
                           cudaStream_t st) {
-  const int64_t U = (int64_t)s.L * s.B * s.Hkv;
-  k_decide<<<(unsigned)U, kDecideThreads, 0, st>>>(s, q, step, warmup_active);
-  return cudaGetLastError();
+  // query rows per thread slot: enough for all rows of one CTA (at most 32 rows)
+  const int rows = units_per_cta(s.G, s.B) * s.G;
+  const int per_slot = (rows + kHashSlots - 1) / kHashSlots;
+  if (per_slot <= 4) return launch_decide_m<4>(s, q, step, warmup_active, st);
+  return launch_decide_m<8>(s, q, step, warmup_active, st);
 }
 
 cudaError_t launch_finish_warmup(const DevState& s, int W, float tau_offset, int n_persist, cudaStream_t st) {

@@ -84,7 +84,7 @@ struct AttSmem {
 };
 
 struct SelSmem {
-  uint16_t scores[kSelChunk];       // scores of the chunk's tokens
+  uint16_t scores[kSelChunkMax];    // scores of the chunk's tokens
   uint32_t hist[kCompWarps][kNBPad]; // histogram of each warp's segment of the chunk
   uint32_t tot[kNBPad];             // the unit's histogram (last chunk to arrive)
   int wc[kCompWarps][2];
@@ -195,7 +195,7 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   return old;
 }
 
-// ---- selection item: one chunk of kSelChunk tokens of one unit --------------------------
+// ---- selection item: one chunk of sel_chunk tokens of one unit -------------------------
 // Scores are small integers (0 .. 128 G), so the top-k is one histogram digit:
 //   1. each warp scores its contiguous quarter of the chunk (16-byte codes read once,
 //      coalesced), keeps the scores in shared memory and builds its own histogram; the
@@ -213,14 +213,14 @@ template <int G>
 __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int gtid) {
   constexpr int NB = 128 * G + 1;
   constexpr int kU = 8;                          // code loads in flight per lane
-  constexpr int WSEG = kSelChunk / kCompWarps;   // tokens per warp
-  static_assert(WSEG % (32 * kU) == 0, "warp segment is whole rounds");
+  const int CH = s.sel_chunk;                    // 8192 or 16384
+  const int WSEG = CH / kCompWarps;              // tokens per warp, a multiple of 32 * kU
   const int NC = s.nch;
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
   const int k = s.kcount[b];
-  const int64_t t0 = (int64_t)c * kSelChunk;
-  const int len = (int)(N - t0 <= 0 ? 0 : (N - t0 < kSelChunk ? N - t0 : kSelChunk));
+  const int64_t t0 = (int64_t)c * CH;
+  const int len = (int)(N - t0 <= 0 ? 0 : (N - t0 < CH ? N - t0 : CH));
   const int warp = gtid >> 5, lane = gtid & 31;
   uint32_t* wh = sm.hist[warp];
   for (int i = lane; i < NB; i += 32) wh[i] = 0;
@@ -257,14 +257,17 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     for (int w = 0; w < kCompWarps; ++w) v += sm.hist[w][i];
     if (v) atomicAdd(UH + i, v);
   }
-  __threadfence();
-  comp_bar();
+  comp_bar();  // the group's additions happen before gtid 0's release below
   if (gtid == 0) sm.misc[0] = atom_add_acq_rel(&s.score_done[u], 1u) == (uint32_t)NC - 1u;
   comp_bar();
 
-  // 2. threshold (last chunk to arrive) or wait for it
+  // 2. threshold (last chunk to arrive) or wait for it.  The last chunk also zeroes the
+  //    unit's histogram for the next step (every chunk has added to it by now).
   if (sm.misc[0]) {
-    for (int i = gtid; i < NB; i += kCompThreads) sm.tot[i] = __ldcg(UH + i);
+    for (int i = gtid; i < NB; i += kCompThreads) {
+      sm.tot[i] = __ldcg(UH + i);
+      UH[i] = 0u;
+    }
     comp_bar();
     if (warp == 0) {
       const int seg = (NB + 31) / 32;
@@ -385,8 +388,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
       off += __popc(bsel);
     }
   }
-  __threadfence();
-  comp_bar();
+  comp_bar();  // the group's index writes happen before gtid 0's release
   if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
 }
 
@@ -463,7 +465,7 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
   // Q^T fragments (B operand): head gid, dims 2*tig (+1, +8, +9) of each k-step
   uint32_t qb[KS][2];
   {
-    const uint16_t* qg = q + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * D;
+    const uint16_t* qg = q + (((int64_t)(l - s.q_l0) * s.B + b) * s.Hq + (int64_t)h * G) * D;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       if (gid < G) {
@@ -637,7 +639,7 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
   // reusing the row buffers), then out[j] = sum_sp w_sp acc_sp[j] / sum_sp w_sp l_sp
   const int np = s.nsplit * kCompWarps;
   const float* pu = s.part + (u * np) * G * (D + 2);
-  float* og = out + (((int64_t)l * s.B + b) * s.Hq + (int64_t)h * G) * D;
+  float* og = out + (((int64_t)(l - s.q_l0) * s.B + b) * s.Hq + (int64_t)h * G) * D;
   float* w = reinterpret_cast<float*>(&sm.rows[0][0][0][0]);  // np floats
   for (int g = 0; g < G; ++g) {
     float mx = -INFINITY;

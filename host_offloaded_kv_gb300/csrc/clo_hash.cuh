@@ -9,8 +9,13 @@
 //   1. fp32 FMA chain s and the chain a = sum |x_i||R_ij|.  Products of two bf16
 //      are exact in fp32 and the FMA chain's error (underflow included) is below
 //      T32 = n * 2^-22 * a + n * 2^-147, so |s| > T32 fixes the sign.
-//   2. fp64: every product is exact and no partial sum can underflow (all are
-//      multiples of 2^-266); error below T64 = n * 2^-51 * a64.
+//   2. compensated fp32 sum of the products: a TwoSum chain whose rounding errors
+//      are summed separately (the "Sum2" scheme of Ogita, Rump and Oishi, "Accurate
+//      sum and dot product", 2005).  Its result r is within eps |s| + g^2 a of the
+//      exact sum (eps = 2^-24, g = (n-1) eps / (1 - (n-1) eps)), plus n * 2^-150
+//      for products that fall below the fp32 normal range, so |r| > 2 g^2 a +
+//      n * 2^-148 fixes the sign.  No fp64: its rate on this GPU is so low that one
+//      fp64 fallback held a whole CTA for ~20 us.
 //   3. fixed point: each product is an integer (< 2^16) times 2^(e - 266) with
 //      0 <= e <= 506, accumulated into 17 int64 limbs of 32 bits; exact.
 // Inputs must be finite; a non-finite element contributes nothing in tier 3.
@@ -59,13 +64,22 @@ static __device__ __noinline__ int exact_dot_sign_bits(const uint32_t* xb, const
 // exactly bf16 (strided accessors), n <= 256.
 template <class XAt, class RAt>
 __device__ __noinline__ bool hash_bit_slow(XAt x, RAt r, int n) {
-  double s = 0.0, a = 0.0;
+  float sh = 0.f, sl = 0.f, a = 0.f;
   for (int i = 0; i < n; ++i) {
-    const double p = (double)x(i) * (double)r(i);
-    s += p;
-    a += fabs(p);
+    const float p = __fmul_rn(x(i), r(i));  // exact unless below the normal range
+    const float t = __fadd_rn(sh, p);       // TwoSum(sh, p) = (t, e), t + e = sh + p exactly
+    const float bp = __fsub_rn(t, sh);
+    const float e = __fadd_rn(__fsub_rn(sh, __fsub_rn(t, bp)), __fsub_rn(p, bp));
+    sh = t;
+    sl = __fadd_rn(sl, e);
+    a = __fadd_rn(a, fabsf(p));
   }
-  if (fabs(s) > (double)n * 4.440892098500626e-16 * a) return s > 0.0;
+  const float res = __fadd_rn(sh, sl);
+  const float nm1 = (float)(n - 1) * 5.9604644775390625e-8f;  // (n - 1) 2^-24
+  const float g = nm1 / (1.f - nm1);
+  // a carries its own rounding (relative error below g): scaled up by 1 + 2g
+  const float bound = 2.f * g * g * (a * (1.f + 2.f * g)) + (float)n * 2.802596928649634e-45f;
+  if (fabsf(res) > bound) return res > 0.f;
   uint32_t xb[256], rb[256];
   for (int i = 0; i < n; ++i) {
     xb[i] = __float_as_uint(x(i)) >> 16;

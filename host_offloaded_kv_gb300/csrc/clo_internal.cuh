@@ -78,18 +78,21 @@ struct DevState {
   int32_t* pers_list;           // [L][B*Hkv] persistent units, per layer
   int32_t* miss_list;           // [L][B*Hkv] missed units, per layer
   unsigned* queue;              // [2] work counters: fetch, compute (zeroed per step)
-  uint32_t* unit_hist;          // [U][nbp] score histogram of each unit being selected (zeroed per step)
+  uint32_t* unit_hist;          // [U][nbp] score histogram of each unit being selected (left zeroed by its last chunk)
   int2* sel_meta;               // [U][nch] {count above T, count at T} of each selection chunk
   int2* sel_thr;                // [U] {threshold score T, count above T}
   uint32_t* score_done;         // [U] chunks whose histogram is merged (zeroed per step)
   uint32_t* fin_done;           // [U] threshold published (zeroed per step)
   uint32_t* cnt_done;           // [U] chunk counts published (zeroed per step)
   uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
-  int nch;                      // selection chunks per unit = ceil(Nmax / kSelChunk)
+  int sel_chunk;                // tokens per selection chunk
+  int nch;                      // selection chunks per unit = ceil(Nmax / sel_chunk)
   int nbp;                      // histogram bins per chunk, padded (>= 128*G + 1)
   unsigned long long* timeline; // [kTimelineSlots] %globaltimer stamps of the step (timing mode), or null
   int64_t wait_timeout_ns;
   int drop_flag_layer;
+  int l0, l1;                   // layers of this launch: [l0, l1)
+  int q_l0;                     // layer of the first [B][Hq][d] block of the q / out buffers
 };
 
 constexpr int kMaxLayers = 256;
@@ -109,9 +112,11 @@ enum Timeline : int {
   TL_SEL_ITEMS = 10,     // selection chunks run
   TL_ATT_SUM_NS = 11,    // summed durations of attention splits (waits included)
   TL_ATT_ITEMS = 12,     // attention splits run
+  TL_DEC_START = 13,     // a CTA of the decide kernel started (first writer)
+  TL_DEC_END = 14,       // last CTA of the decide kernel finished
   kTimelineSlots = 16
 };
-constexpr int kSelChunk = 8192;  // tokens per selection chunk
+constexpr int kSelChunkMax = 16384;  // tokens per selection chunk, at most (8192 or 16384)
 constexpr int kPartsPerSplit = 4; // attention partials per split (one per compute warp)
 constexpr int kSplitRows = 1024;  // selected rows per attention split
 constexpr int kChunkRows = 256;   // selected rows per fetch chunk (one ready flag each)

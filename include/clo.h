@@ -156,6 +156,22 @@ CLO_API clo_status clo_append_kv(clo_ctx* ctx, int32_t layer, int32_t seq, const
  * CLO_ERR_CUDA, CLO_ERR_TIMEOUT / CLO_ERR_DEVICE (host-buffer mode only). */
 CLO_API clo_status clo_decode_step(clo_ctx* ctx, const void* q, float* out, int32_t io_on_device);
 
+/* One layer of a decode step, for callers whose layer l+1 query exists only after
+ * layer l's output (a model running layer by layer).  CLO prefetches one layer ahead
+ * ([SYN] 5.6); here the rows of every unit's last selection stay in its on-GPU cache
+ * slot between steps, so a reused unit needs no transfer at all and a unit that
+ * misses needs its new query first.  The call runs the reuse test, selection, fetch
+ * and attention of `layer` only, enqueued on the context's stream.
+ * q: bf16 [B][Hq][d] of this layer; out: fp32 [B][Hq][d] of this layer; io_on_device
+ * as for clo_decode_step.  Layers must come in order 0, 1, ..., L-1; the step (warm-up
+ * counting, statistics) completes with layer L-1.  A sequence of clo_decode_layer
+ * calls over all layers computes exactly what one clo_decode_step computes.
+ * Errors: CLO_ERR_INVALID (null pointer, layer out of range), CLO_ERR_STATE (layer
+ * out of order, no K/V, ragged layers), CLO_ERR_CUDA, CLO_ERR_TIMEOUT /
+ * CLO_ERR_DEVICE (host-buffer mode only).  clo_decode_step and clo_append_kv return
+ * CLO_ERR_STATE while a layer-by-layer step is in progress. */
+CLO_API clo_status clo_decode_layer(clo_ctx* ctx, int32_t layer, const void* q, float* out, int32_t io_on_device);
+
 /* Wait for all work of the context and report a latched device error, if any
  * (CLO_ERR_TIMEOUT or CLO_ERR_DEVICE); the latch is cleared once reported. */
 CLO_API clo_status clo_sync(clo_ctx* ctx);
@@ -187,7 +203,8 @@ CLO_API const char* clo_last_error(void);
  *                       attention split done, [7] summed fetch waits on selections,
  *                       [8] summed attention waits on fetch flags, [9] summed durations
  *                       of selection chunks, [10] their number, [11] summed durations
- *                       of attention splits, [12] their number
+ *                       of attention splits, [12] their number, [13] first CTA of
+ *                       the step's decide kernel started, [14] its last CTA finished
  * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,

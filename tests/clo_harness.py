@@ -90,7 +90,9 @@ class LockStep:
             want = self.orc.kcodes[u]
             assert np.array_equal(got, want), f"key codes differ for unit {u}"
 
-    def step(self, q=None, check=True, io_on_device=True):
+    def step(self, q=None, check=True, io_on_device=True, per_layer=False):
+        """One decode step through clo_decode_step, or (per_layer) through one
+        clo_decode_layer call per layer; the oracle takes the whole step."""
         torch = self.torch
         s = self.spec
         if q is None:
@@ -98,12 +100,20 @@ class LockStep:
         if io_on_device:
             qd = torch.from_numpy(q.view(np.int16)).cuda()
             outd = torch.empty((s.L, s.B, s.Hq, s.d), dtype=torch.float32, device="cuda")
-            self.lib.decode_step(qd, outd)
+            if per_layer:
+                for l in range(s.L):
+                    self.lib.decode_layer(l, qd[l], outd[l])
+            else:
+                self.lib.decode_step(qd, outd)
             self.lib.sync()
             out = outd.cpu().numpy()
         else:
             out = np.empty((s.L, s.B, s.Hq, s.d), dtype=np.float32)
-            self.lib.decode_step(q, out, io_on_device=False)
+            if per_layer:
+                for l in range(s.L):
+                    self.lib.decode_layer(l, np.ascontiguousarray(q[l]), out[l], io_on_device=False)
+            else:
+                self.lib.decode_step(q, out, io_on_device=False)
         dec = self.lib.decisions()
         stats = self.lib.stats()
         dev_persist = self.lib.persist()

@@ -78,3 +78,35 @@ def test_all_scores_tied_selects_lowest_indices(N, topk):
         assert ls.lib.idx(0, 0, 0).tolist() == list(range(k))
     finally:
         ls.close()
+
+
+def test_hash_cancellations_take_the_exact_tiers():
+    # keys built from the projection's own columns: token t uses column j = t % 128 and
+    # x = (R[1, j], -R[0, j], c, 0, ...), whose dot with column j is exactly c * R[2, j]:
+    # c = 0 (exact zero: bit 0), c = 2^-18 (too small for the fp32 chain's bound, settled
+    # by the compensated sum) or c = 2^-40 (below that bound too: settled by the exact
+    # fixed-point tier).  Codes must match the oracle bit for bit.
+    from host_offloaded_kv_gb300.synth import Synth
+
+    L, B, Hkv, d, N, seed = 1, 1, 1, 64, 768, 21
+    R = Synth(seed, 0.01).hash_matrices(L, Hkv, d)[0, 0]   # bf16 bits [d][128]
+    K = np.zeros((N, Hkv, d), dtype=np.uint16)
+    tiny = {0: 0, 1: 0x3680, 2: 0x2B80}                      # bf16 bits of 0, 2^-18, 2^-40
+    for t in range(N):
+        j = t % 128
+        K[t, 0, 0] = R[1, j]
+        K[t, 0, 1] = R[0, j] ^ 0x8000
+        K[t, 0, 2] = tiny[(t // 128) % 3]
+    V = np.zeros((N, Hkv, d), dtype=np.uint16)
+    V[:, :, :] = (np.arange(N, dtype=np.uint16)[:, None, None] % 977 + 0x3c00) & 0x7fff
+    spec = Spec(L=L, B=B, Hq=2, Hkv=Hkv, d=d, ntok=[N], seed=seed, tau=2.0, kv_override={(0, 0): (K, V)})
+    ls = LockStep(spec)
+    try:
+        ls.check_key_codes()
+        codes = ls.lib.key_codes(0, 0, 0)
+        bits = np.unpackbits(codes.view(np.uint8), bitorder="little").reshape(N, 128)
+        zero_rows = [t for t in range(N) if (t // 128) % 3 == 0]
+        assert not bits[zero_rows, np.array(zero_rows) % 128].any()  # exact zeros give bit 0
+        ls.step()
+    finally:
+        ls.close()
