@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--batch", type=int, default=0,
                    help="override the batch (for workloads whose host pool exceeds the box's memory)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--adaptive-tau", action="store_true",
+                   help="online adaptive thresholds after warm-up (running average of the live cosines)")
     p.add_argument("--layerwise", action="store_true",
                    help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -227,7 +229,7 @@ def run_gb300(args, rank, world, local_rank):
     lib = CLOContext(n_layers=L, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, max_tokens=N, hash_R=R,
                      topk=w.topk, topk_ratio=w.topk_ratio, tau=tau, warmup_steps=w.warmup_steps,
                      tau_offset=w.tau_offset, n_persist=w.n_persist if tau is None else 0, timing=True,
-                     stream=stream.cuda_stream)
+                     stream=stream.cuda_stream, adaptive_tau=args.adaptive_tau)
     if args.layerwise:
         def step_fn(q, o, io_on_device=None):
             for l in range(L):
@@ -354,8 +356,9 @@ def run_gb300(args, rank, world, local_rank):
         "dtype": "f32", "data": "synthetic (seeded generator; N(0,1) bf16 K/V, 1% heavy hitters, AR(1) queries)",
         "config": {"workload": w.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
                    "head_dim": d, "context": N, "topk": kmax, "persistent_heads": w.n_persist if tau is None else 0,
-                   "tau": f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
-                   else w.tau_fixed, "kv_dtype": "bf16", "parallelism": f"replicas x{world} (independent sequences)",
+                   "tau": (f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
+                           else w.tau_fixed) + (", then adaptive (running average, weight 1/16)"
+                                                if args.adaptive_tau else ""), "kv_dtype": "bf16", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1),

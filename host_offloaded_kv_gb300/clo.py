@@ -54,6 +54,8 @@ class clo_config(ctypes.Structure):
         ("timing", ctypes.c_int32),
         ("debug_drop_flag_layer", ctypes.c_int32),
         ("stream", ctypes.c_void_p),
+        ("adaptive_tau", ctypes.c_int32),
+        ("tau_ema", ctypes.c_double),
     ]
 
 
@@ -207,7 +209,7 @@ class CLOContext:
 
     def __init__(self, *, n_layers, batch, n_q_heads, n_kv_heads, head_dim, max_tokens, hash_R, topk=0,
                  topk_ratio=0.1, tau=None, persist_mask=None, warmup_steps=16, tau_offset=0.05, n_persist=0,
-                 wait_timeout_ns=2_000_000_000, timing=False, stream=None):
+                 wait_timeout_ns=2_000_000_000, timing=False, stream=None, adaptive_tau=False, tau_ema=0.0625):
         self.L, self.B, self.Hq, self.Hkv, self.d = n_layers, batch, n_q_heads, n_kv_heads, head_dim
         self.G = n_q_heads // n_kv_heads
         self.topk, self.topk_ratio = int(topk), float(topk_ratio)
@@ -230,6 +232,8 @@ class CLOContext:
         cfg.timing = int(bool(timing))
         cfg.debug_drop_flag_layer = -1
         cfg.stream = stream
+        cfg.adaptive_tau = int(bool(adaptive_tau))
+        cfg.tau_ema = float(tau_ema)
         self.cfg = cfg
         self.ctx = clo_init(cfg)
         self.ntok = np.zeros((n_layers, batch), dtype=np.int64)

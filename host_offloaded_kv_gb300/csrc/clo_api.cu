@@ -119,6 +119,7 @@ CLO_API void clo_config_default(clo_config* cfg) {
   cfg->tau_offset = 0.05f;
   cfg->wait_timeout_ns = 2000000000LL;
   cfg->debug_drop_flag_layer = -1;
+  cfg->tau_ema = 0.0625;
 }
 
 CLO_API const char* clo_last_error(void) { return g_last_error.c_str(); }
@@ -141,6 +142,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   if (cfg->topk < 0) return fail(CLO_ERR_INVALID, "topk must be >= 0");
   if (cfg->topk == 0 && !(cfg->topk_ratio > 0.0 && cfg->topk_ratio <= 1.0))
     return fail(CLO_ERR_INVALID, "topk_ratio must be in (0, 1] when topk == 0");
+  if (cfg->adaptive_tau && !(cfg->tau_ema > 0.0 && cfg->tau_ema <= 1.0))
+    return fail(CLO_ERR_INVALID, "tau_ema must be in (0, 1] with adaptive_tau");
   c->warmup_mode = cfg->tau == nullptr;
   if (c->warmup_mode) {
     if (cfg->warmup_steps < 2) return fail(CLO_ERR_INVALID, "warmup_steps must be >= 2 when tau is NULL");
@@ -269,6 +272,19 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   CLO_TRY(c->dalloc(&s.pers_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.miss_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.unit_hist, (size_t)U * s.nbp));
+  s.tau_ema = cfg->tau_ema;
+  s.tau_offset = cfg->tau_offset;
+  if (cfg->adaptive_tau) {
+    CLO_TRY(c->dalloc(&s.qprev, (size_t)U * c->G * c->d));
+    CLO_TRY(c->dalloc(&s.qprev_valid, (size_t)U));
+    CLO_TRY(c->dalloc(&s.cos_sum, (size_t)LH));
+    CLO_TRY(c->dalloc(&s.cos_cnt, (size_t)LH));
+  } else {
+    s.qprev = nullptr;
+    s.qprev_valid = nullptr;
+    s.cos_sum = nullptr;
+    s.cos_cnt = nullptr;
+  }
   CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * s.nch));
   CLO_TRY(c->dalloc(&s.sel_thr, (size_t)U));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
@@ -280,6 +296,11 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   std::vector<uint8_t> pm((size_t)LH, 0);
   if (!c->warmup_mode) {
     CLO_CUDA(cudaMemcpy(s.tau, cfg->tau, sizeof(float) * LH, cudaMemcpyHostToDevice));
+    if (cfg->adaptive_tau) {  // the running average starts from the given thresholds
+      std::vector<double> sh((size_t)LH);
+      for (int i = 0; i < LH; ++i) sh[(size_t)i] = (double)cfg->tau[i] + (double)cfg->tau_offset;
+      CLO_CUDA(cudaMemcpy(s.shat, sh.data(), sizeof(double) * LH, cudaMemcpyHostToDevice));
+    }
     if (cfg->persist_mask) {
       for (int l = 0; l < c->L; ++l) {
         int p = 0;
@@ -401,6 +422,7 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   s.l1 = l1;
   s.q_l0 = l0;
   const bool warm = c->warmup_mode && c->step < c->W;
+  s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
   const bool timed = c->cfg.timing != 0;
   cudaEvent_t* ev = nullptr;
   if (timed) {

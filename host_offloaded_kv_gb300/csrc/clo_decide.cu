@@ -107,6 +107,37 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
     nq = warp_sum(nq);
     nc = warp_sum(nc);
     const float cosv = (nq > 0.f && nc > 0.f) ? dot / (sqrtf(nq) * sqrtf(nc)) : 0.f;
+    if (s.qprev) {  // adaptive thresholds: cos(q_t, q_{t-1}); q_t becomes the previous query
+      uint16_t* qp = s.qprev + u * GD;
+      const bool pvalid = s.qprev_valid[u] != 0;
+      float pd = 0.f, pn = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxPer; ++p) {
+        const int e = 8 * lane + 256 * p;
+        if (e < GD) {
+          const uint4 pv = *reinterpret_cast<const uint4*>(qp + e);
+          const uint32_t xw[4] = {xv[p].x, xv[p].y, xv[p].z, xv[p].w}, pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x0 = bf16_bits_to_f32(xw[i] & 0xffffu), x1 = bf16_bits_to_f32(xw[i] >> 16);
+            const float p0 = bf16_bits_to_f32(pw[i] & 0xffffu), p1 = bf16_bits_to_f32(pw[i] >> 16);
+            pd = fmaf(x1, p1, fmaf(x0, p0, pd));
+            pn = fmaf(p1, p1, fmaf(p0, p0, pn));
+          }
+          *reinterpret_cast<uint4*>(qp + e) = xv[p];
+        }
+      }
+      pd = warp_sum(pd);
+      pn = warp_sum(pn);
+      if (lane == 0) {
+        if (pvalid && s.adapt_active) {
+          const float cp = (nq > 0.f && pn > 0.f) ? pd / (sqrtf(nq) * sqrtf(pn)) : 0.f;
+          atomicAdd(&s.cos_sum[lh], (double)cp);
+          atomicAdd(&s.cos_cnt[lh], 1u);
+        }
+        s.qprev_valid[u] = 1;
+      }
+    }
     int dec;
     if (warmup_active)
       dec = CLO_DEC_MISS;

@@ -783,6 +783,20 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     sec_start[0] = 0;
     for (int i = 0; i < 5; ++i) sec_start[i + 1] = sec_start[i] + size[i];
   }
+  if (s.adapt_active && blockIdx.x == 0) {
+    // online thresholds: fold this step's mean adjacent-step cosine of each (layer,
+    // kv head) into s_hat; the decide kernel, finished before this launch, summed them
+    for (int lh = s.l0 * s.Hkv + tid; lh < s.l1 * s.Hkv; lh += blockDim.x) {
+      const uint32_t n = s.cos_cnt[lh];
+      if (n) {
+        const double sh = (1.0 - s.tau_ema) * s.shat[lh] + s.tau_ema * (s.cos_sum[lh] / (double)n);
+        s.shat[lh] = sh;
+        s.tau[lh] = (float)(sh - (double)s.tau_offset);
+      }
+      s.cos_sum[lh] = 0.0;
+      s.cos_cnt[lh] = 0u;
+    }
+  }
   __syncthreads();
   if (warp < FW) {
     fetch_role<D, FU>(s, pre[2], pre[2][L], lane, fidx[warp]);

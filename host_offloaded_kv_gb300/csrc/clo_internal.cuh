@@ -91,6 +91,13 @@ struct DevState {
   unsigned long long* timeline; // [kTimelineSlots] %globaltimer stamps of the step (timing mode), or null
   int64_t wait_timeout_ns;
   int drop_flag_layer;
+  uint16_t* qprev;              // [U][G*d] query of the previous step (adaptive thresholds), or null
+  uint8_t* qprev_valid;         // [U]
+  double* cos_sum;              // [L*Hkv] sum over the step's units of cos(q_t, q_{t-1})
+  uint32_t* cos_cnt;            // [L*Hkv] number of terms in cos_sum
+  int adapt_active;             // this launch updates s_hat and tau from cos_sum
+  double tau_ema;               // weight of the newest step in the s_hat average
+  float tau_offset;             // tau = s_hat - tau_offset
   int l0, l1;                   // layers of this launch: [l0, l1)
   int q_l0;                     // layer of the first [B][Hq][d] block of the q / out buffers
 };

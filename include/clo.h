@@ -98,6 +98,15 @@ typedef struct clo_config {
   int32_t debug_drop_flag_layer; /* fault injection: >= 0 -> the fetch of this layer
                                     never signals its ready flags; -1 = off */
   void* stream;            /* cudaStream_t to run on; NULL = the legacy default stream */
+  /* online adaptive thresholds ([SYN] 5.3: online adaptation instead of offline
+   * profiling only): nonzero -> after warm-up (or from the first step with fixed tau,
+   * starting from s_hat = tau + tau_offset), every step updates, per (layer, kv head),
+   *   s_hat = (1 - tau_ema) * s_hat + tau_ema * m,   tau = s_hat - tau_offset,
+   * where m is the mean over the batch of cos(q_t, q_{t-1}) (the group's
+   * concatenated queries at this step and the previous one); the new tau applies
+   * from the next step.  Persistent heads stay as chosen.  0 = off (default). */
+  int32_t adaptive_tau;
+  double tau_ema;          /* weight of the newest step, in (0, 1]; default 1/16 */
 } clo_config;
 
 typedef struct clo_stats_t {
@@ -121,7 +130,7 @@ typedef struct clo_stats_t {
 } clo_stats_t;
 
 /* Fill *cfg with defaults (shapes zero; topk_ratio 0.1; warmup_steps 16;
- * tau_offset 0.05; wait 2 s; debug_drop_flag_layer -1). */
+ * tau_offset 0.05; wait 2 s; debug_drop_flag_layer -1; adaptive_tau 0, tau_ema 1/16). */
 CLO_API void clo_config_default(clo_config* cfg);
 
 /* Create a context: allocates the pinned, device-mapped host K/V pool

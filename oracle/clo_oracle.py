@@ -171,7 +171,7 @@ class OracleCLO:
     units (they need only the queries)."""
 
     def __init__(self, L, B, Hq, Hkv, d, R, *, topk=0, topk_ratio=0.1, tau=None, persist_mask=None,
-                 warmup_steps=16, tau_offset=0.05, n_persist=0, ntok=None):
+                 warmup_steps=16, tau_offset=0.05, n_persist=0, ntok=None, adaptive_tau=False, tau_ema=0.0625):
         load_oracle()
         assert Hq % Hkv == 0
         self.L, self.B, self.Hq, self.Hkv, self.d = L, B, Hq, Hkv, d
@@ -201,6 +201,14 @@ class OracleCLO:
         self.shat_sum = np.zeros((L, Hkv), dtype=np.float64)
         self.shat = None
         self.persist_ambiguous = False
+        # online adaptive thresholds ("CLO (2511.14510) - L3 Per-Paper Synthesis",
+        # section 5.3): s_hat follows the live adjacent-step cosines after warm-up
+        self.adaptive = bool(adaptive_tau)
+        self.ema = float(tau_ema)
+        self.qprev = np.zeros((L, B, Hkv, self.G * d), dtype=np.uint16)
+        self.qprev_valid = np.zeros((L, B, Hkv), dtype=bool)
+        if self.adaptive and not self.warmup:
+            self.shat = self.tau + self.tau_offset
 
     # context -------------------------------------------------------------------
     def set_unit_kv(self, l, b, h, K, V):
@@ -267,10 +275,26 @@ class OracleCLO:
             idx = self.sel[u]
             res.idx[u] = idx
             res.out[u] = attention(qr[l, b, h], K[idx], V[idx])
+        if self.adaptive:
+            if not in_warmup:
+                self._adapt_tau(q)
+            self.qprev[...] = q
+            self.qprev_valid[...] = True
         if in_warmup and self.t == self.W - 1:
             self._finish_warmup(device_persist)
         self.t += 1
         return res
+
+    def _adapt_tau(self, q):
+        """s_hat[l, h] <- (1 - a) s_hat + a * mean_b cos(q_t, q_{t-1}), tau = s_hat - offset;
+        the new tau applies from the next step."""
+        for l in range(self.L):
+            for h in range(self.Hkv):
+                vals = [cosine(q[l, b, h], self.qprev[l, b, h]) for b in range(self.B) if self.qprev_valid[l, b, h]]
+                if vals:
+                    m = sum(vals) / len(vals)
+                    self.shat[l, h] = (1.0 - self.ema) * self.shat[l, h] + self.ema * m
+                    self.tau[l, h] = self.shat[l, h] - self.tau_offset
 
     def _finish_warmup(self, device_persist=None):
         npairs = self.B * (self.W - 1)

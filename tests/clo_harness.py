@@ -40,6 +40,8 @@ class Spec:
     max_tokens: int | None = None
     sample: list | None = None   # units (l, b, h) given to the oracle; None = all
     kv_override: dict = field(default_factory=dict)  # (l, b) -> (K, V) replacing generated data
+    adaptive_tau: bool = False
+    tau_ema: float = 0.0625
 
 
 class LockStep:
@@ -57,10 +59,11 @@ class LockStep:
         self.lib = CLOContext(n_layers=s.L, batch=s.B, n_q_heads=s.Hq, n_kv_heads=s.Hkv, head_dim=s.d,
                               max_tokens=maxtok, hash_R=self.R, topk=s.topk, topk_ratio=s.topk_ratio, tau=tau,
                               persist_mask=s.persist_mask, warmup_steps=s.warmup_steps, tau_offset=s.tau_offset,
-                              n_persist=s.n_persist)
+                              n_persist=s.n_persist, adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema)
         self.orc = orc.OracleCLO(s.L, s.B, s.Hq, s.Hkv, s.d, self.R, topk=s.topk, topk_ratio=s.topk_ratio,
                                  tau=tau, persist_mask=s.persist_mask, warmup_steps=s.warmup_steps,
-                                 tau_offset=s.tau_offset, n_persist=s.n_persist, ntok=s.ntok)
+                                 tau_offset=s.tau_offset, n_persist=s.n_persist, ntok=s.ntok,
+                                 adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema)
         units = s.sample if s.sample is not None else [
             (l, b, h) for l in range(s.L) for b in range(s.B) for h in range(s.Hkv)]
         self.units = list(units)
@@ -127,6 +130,8 @@ class LockStep:
         assert np.array_equal(dec.astype(np.int8), res.decision), (
             f"step {res.step}: decisions differ at {np.argwhere(dec.astype(np.int8) != res.decision)[:5]}")
         assert stats["last_host_bytes"] == res.host_bytes, (stats["last_host_bytes"], res.host_bytes)
+        if s.adaptive_tau and self.orc.tau is not None:   # thresholds after this step's update
+            np.testing.assert_allclose(self.lib.tau(), self.orc.tau, atol=1e-5, rtol=0)
         G, d = self.G, s.d
         qr = q.reshape(s.L, s.B, s.Hkv, G, d)
         for u in self.units:

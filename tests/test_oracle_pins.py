@@ -372,3 +372,47 @@ def test_state_excused_band_follows_device():
     r = o.step(q1, device_decision=dev)
     assert r.excused[0, 0, 0] and r.decision[0, 0, 0] == orc.DEC_HIT
     assert r.excused.sum() == 1
+
+
+def _adaptive_small(tau0, ema):
+    L, B, Hq, Hkv, d = 1, 2, 4, 2, 16
+    syn = Synth(41)
+    R = syn.hash_matrices(L, Hkv, d)
+    o = orc.OracleCLO(L, B, Hq, Hkv, d, R, topk_ratio=0.1, tau=np.full(L * Hkv, tau0, dtype=np.float32),
+                      tau_offset=0.05, adaptive_tau=True, tau_ema=ema)
+    return o, syn.normal_bf16(0, L * B * Hq * d).reshape(L, B, Hq, d)
+
+
+def test_adaptive_tau_closed_form_geometric_decay():
+    # sequence 0 repeats its query (cos 1), sequence 1 flips its sign each step
+    # (cos -1): the batch mean is 0, so s_hat_n = s_hat_0 (1 - a)^n after the first step
+    a = 0.25
+    o, q = _adaptive_small(0.3, a)
+    s0 = float(np.float32(0.3)) + 0.05
+    assert np.allclose(o.shat, s0, rtol=0, atol=1e-15)
+    for t in range(6):
+        qt = q.copy()
+        if t % 2:
+            qt[:, 1] ^= 0x8000
+        tau_before = o.tau.copy()
+        o.step(qt)
+        n = max(0, t)            # no previous query at step 0: no update
+        want = s0 * (1 - a) ** n
+        assert np.allclose(o.shat, want, rtol=0, atol=1e-12), (t, o.shat, want)
+        assert np.allclose(o.tau, want - 0.05, rtol=0, atol=1e-12)
+        if t == 0:
+            assert np.array_equal(o.tau, tau_before)
+
+
+def test_adaptive_tau_closed_form_converges_to_one():
+    # both sequences repeat their queries: m = 1, s_hat_n = 1 - (1 - a)^n (1 - s_hat_0)
+    a = 0.5
+    o, q = _adaptive_small(0.1, a)
+    s0 = float(np.float32(0.1)) + 0.05
+    for t in range(5):
+        o.step(q)
+        want = 1.0 - (1 - a) ** t * (1.0 - s0)
+        assert np.allclose(o.shat, want, rtol=0, atol=1e-12)
+    # with tau near 1 - 0.05 every reused head now hits (cos = 1 >= tau)
+    r = o.step(q)
+    assert np.all(r.decision == orc.DEC_HIT)
