@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--adaptive-tau", action="store_true",
                    help="online adaptive thresholds after warm-up (running average of the live cosines)")
+    p.add_argument("--kv-bits", type=int, default=16, choices=[16, 4, 2],
+                   help="host pool storage: bf16, or 4/2-bit asymmetric codes dequantised on the GPU")
     p.add_argument("--layerwise", action="store_true",
                    help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -78,26 +80,45 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
+        self.reader = None
 
-    def start(self):
+    def start(self, wait_samples: int = 2, timeout_s: float = 10.0):
+        """Starts nvidia-smi polling and returns once it has delivered wait_samples
+        samples, so that its start-up (driver queries) is over before timing begins."""
+        import threading
+
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
                  "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.15)
+            return
+
+        def read():
+            for line in self.proc.stdout:
+                self.lines.append(line)
+
+        self.reader = threading.Thread(target=read, daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while len(self.lines) < wait_samples and time.time() - t0 < timeout_s and self.proc.poll() is None:
+            time.sleep(0.02)
+        self.skip = len(self.lines)   # samples taken before the timed region
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        time.sleep(0.1)
+        time.sleep(0.25)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+            self.proc.wait()
+        self.reader.join(timeout=5)
+        out = "".join(self.lines[self.skip:])
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -216,7 +237,8 @@ def run_gb300(args, rank, world, local_rank):
 
     w = workload_from_args(args)
     L, B, Hq, Hkv, d, N = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_tokens
-    pool_bytes = L * B * Hkv * N * 4 * d
+    rec_bytes = 4 * d if args.kv_bits == 16 else 2 * d * args.kv_bits // 8 + (2 * d // 64) * 8
+    pool_bytes = L * B * Hkv * N * rec_bytes
     if mem_available_bytes() < pool_bytes * 1.15 + (1 << 30):
         raise SystemExit(f"not enough host memory for the {pool_bytes / 2**30:.1f} GiB pinned pool of {w.name}")
     torch.cuda.set_device(local_rank)
@@ -229,7 +251,7 @@ def run_gb300(args, rank, world, local_rank):
     lib = CLOContext(n_layers=L, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, max_tokens=N, hash_R=R,
                      topk=w.topk, topk_ratio=w.topk_ratio, tau=tau, warmup_steps=w.warmup_steps,
                      tau_offset=w.tau_offset, n_persist=w.n_persist if tau is None else 0, timing=True,
-                     stream=stream.cuda_stream, adaptive_tau=args.adaptive_tau)
+                     stream=stream.cuda_stream, adaptive_tau=args.adaptive_tau, kv_bits=args.kv_bits)
     if args.layerwise:
         def step_fn(q, o, io_on_device=None):
             for l in range(L):
@@ -257,6 +279,9 @@ def run_gb300(args, rank, world, local_rank):
         qdev[i].copy_(torch.from_numpy(qh.view(np.int16)))
     out = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
+    # the link peak is measured before the warm-up steps: large pinned copies evict the
+    # device's translations of host pages, and the first steps after them refill those
+    link_gbs_before = pinned_h2d_gbs(dev)
     with torch.cuda.stream(stream):
         for i in range(n_prof + W):
             step_fn(qdev[i], out)
@@ -264,7 +289,6 @@ def run_gb300(args, rank, world, local_rank):
     lib.stats()  # drops the per-phase events of untimed steps
     before = lib.stats()
 
-    link_gbs_before = pinned_h2d_gbs(dev)
     sampler = ClockSampler(local_rank)
     sampler.start()
     if world > 1:
@@ -358,7 +382,8 @@ def run_gb300(args, rank, world, local_rank):
                    "head_dim": d, "context": N, "topk": kmax, "persistent_heads": w.n_persist if tau is None else 0,
                    "tau": (f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
                            else w.tau_fixed) + (", then adaptive (running average, weight 1/16)"
-                                                if args.adaptive_tau else ""), "kv_dtype": "bf16", "parallelism": f"replicas x{world} (independent sequences)",
+                                                if args.adaptive_tau else ""), "kv_dtype": "bf16" if args.kv_bits == 16 else
+                   f"int{args.kv_bits} host pool (asymmetric, 64-channel groups, fp32 scale/min), bf16 on the GPU", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1),

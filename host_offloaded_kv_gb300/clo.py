@@ -56,6 +56,7 @@ class clo_config(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("adaptive_tau", ctypes.c_int32),
         ("tau_ema", ctypes.c_double),
+        ("kv_bits", ctypes.c_int32),
     ]
 
 
@@ -209,7 +210,8 @@ class CLOContext:
 
     def __init__(self, *, n_layers, batch, n_q_heads, n_kv_heads, head_dim, max_tokens, hash_R, topk=0,
                  topk_ratio=0.1, tau=None, persist_mask=None, warmup_steps=16, tau_offset=0.05, n_persist=0,
-                 wait_timeout_ns=2_000_000_000, timing=False, stream=None, adaptive_tau=False, tau_ema=0.0625):
+                 wait_timeout_ns=2_000_000_000, timing=False, stream=None, adaptive_tau=False, tau_ema=0.0625,
+                 kv_bits=16):
         self.L, self.B, self.Hq, self.Hkv, self.d = n_layers, batch, n_q_heads, n_kv_heads, head_dim
         self.G = n_q_heads // n_kv_heads
         self.topk, self.topk_ratio = int(topk), float(topk_ratio)
@@ -234,6 +236,8 @@ class CLOContext:
         cfg.stream = stream
         cfg.adaptive_tau = int(bool(adaptive_tau))
         cfg.tau_ema = float(tau_ema)
+        cfg.kv_bits = int(kv_bits)
+        self.kv_bits = int(kv_bits)
         self.cfg = cfg
         self.ctx = clo_init(cfg)
         self.ntok = np.zeros((n_layers, batch), dtype=np.int64)
@@ -321,4 +325,5 @@ class CLOContext:
                 "selection_chunk_mean_us": round(int(t[9]) / 1e3 / max(1, int(t[10])), 2),
                 "selection_chunks": int(t[10]),
                 "attention_split_mean_us": round(int(t[11]) / 1e3 / max(1, int(t[12])), 2),
-                "attention_splits": int(t[12]), "decide_start_us": rel(t[13]), "decide_end_us": rel(t[14])}
+                "attention_splits": int(t[12]), "decide_start_us": rel(t[13]), "decide_end_us": rel(t[14]),
+                "attention_split_run_mean_us": round(int(t[15]) / 1e3 / max(1, int(t[12])), 2)}

@@ -59,6 +59,7 @@ struct clo_ctx {
   int64_t* ntok_pinned = nullptr;  // [B] + k [B] staging for uploads
   int64_t step = 0;
   bool warmup_mode = false;
+  int kv_bits = 16;
   int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
   int W = 0;
   bool warmup_done = false;
@@ -142,6 +143,9 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   if (cfg->topk < 0) return fail(CLO_ERR_INVALID, "topk must be >= 0");
   if (cfg->topk == 0 && !(cfg->topk_ratio > 0.0 && cfg->topk_ratio <= 1.0))
     return fail(CLO_ERR_INVALID, "topk_ratio must be in (0, 1] when topk == 0");
+  c->kv_bits = cfg->kv_bits == 0 ? 16 : cfg->kv_bits;
+  if (c->kv_bits != 16 && c->kv_bits != 4 && c->kv_bits != 2)
+    return fail(CLO_ERR_INVALID, "kv_bits must be 16, 4 or 2");
   if (cfg->adaptive_tau && !(cfg->tau_ema > 0.0 && cfg->tau_ema <= 1.0))
     return fail(CLO_ERR_INVALID, "tau_ema must be in (0, 1] with adaptive_tau");
   c->warmup_mode = cfg->tau == nullptr;
@@ -176,8 +180,9 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   CLO_CUDA(cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev));
   if (!can_map) return fail(CLO_ERR_CUDA, "device cannot map host memory");
 
-  // pinned, device-mapped host pool: [U][Nmax][K|V]
-  const size_t rec = (size_t)4 * c->d;
+  // pinned, device-mapped host pool: [U][Nmax][K|V record]
+  const size_t rec = c->kv_bits == 16 ? (size_t)4 * c->d
+                                      : (size_t)2 * c->d * c->kv_bits / 8 + (size_t)(2 * c->d / 64) * 8;
   const size_t pool_bytes = (size_t)c->U * (size_t)c->Nmax * rec;
   void* hp = nullptr;
   cudaError_t e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -199,6 +204,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   s.Nmax = c->Nmax;
   s.kmax = c->kmax;
   s.pool = static_cast<const uint16_t*>(pd);
+  s.kv_bits = c->kv_bits;
+  s.rec_bytes = (int)rec;
   s.wait_timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : 2000000000LL;
   s.drop_flag_layer = cfg->debug_drop_flag_layer;
   s.nsplit = (int)((c->kmax + kSplitRows - 1) / kSplitRows);
@@ -235,9 +242,9 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   }
   // per-step zeroed region: step counters, per-layer list lengths, work queues, ready
   // flags of the fetch chunks, selection progress counters
-  // selection chunks: 8192 tokens up to 32K contexts (enough chunks per unit to select a
-  // unit quickly), 16384 beyond (fewer threshold hand-offs per token)
-  s.sel_chunk = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
+  // selection: contexts up to 32K tokens are selected whole by one compute group (the
+  // scores fit in its shared memory); longer ones in chunks of 16384 tokens by several
+  s.sel_chunk = c->Nmax <= 32768 ? (int)c->Nmax : kSelChunkMax;
   s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
   s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
   {

@@ -100,6 +100,82 @@ __global__ void k_pool_write(DevState s, int l, int b, int64_t t0, int64_t n, co
   }
 }
 
+// Quantised pool write: one thread per (token, kv head, K or V, 64-channel group).
+//   mn, mx of the group; scale = (mx - mn) / (2^BITS - 1);
+//   q = clamp(rint((x - mn) / scale), 0, 2^BITS - 1), 0 when scale is 0
+// (every operation fp32, rounded to nearest).  The codes and (scale, mn) go to the
+// token's record; a persistent head's resident copy gets the dequantised values.
+template <int D, int BITS>
+__global__ void k_pool_write_q(DevState s, int l, int b, int64_t t0, int64_t n, const uint16_t* __restrict__ K,
+                               const uint16_t* __restrict__ V) {
+  using Q = QRec<D, BITS>;
+  constexpr int NG = D / 64;  // groups per row
+  constexpr float kLevels = (float)((1 << BITS) - 1);
+  const int64_t total = n * s.Hkv * 2 * NG;
+  unsigned char* pool = reinterpret_cast<unsigned char*>(const_cast<uint16_t*>(s.pool));
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+    const int g = (int)(e % NG);
+    const int kv = (int)((e / NG) % 2);
+    const int h = (int)((e / (2 * NG)) % s.Hkv);
+    const int64_t t = e / (2 * (int64_t)NG * s.Hkv);
+    const uint4* src = reinterpret_cast<const uint4*>((kv == 0 ? K : V) + (t * s.Hkv + h) * D + 64 * g);
+    float x[64];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const uint4 w = src[v];
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * v + 2 * i] = bf16_bits_to_f32(ww[i] & 0xffffu);
+        x[8 * v + 2 * i + 1] = bf16_bits_to_f32(ww[i] >> 16);
+      }
+    }
+    float mn = x[0], mx = x[0];
+#pragma unroll
+    for (int i = 1; i < 64; ++i) {
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
+    }
+    mn = __fadd_rn(mn, 0.f);  // a zero minimum is +0 whichever zero fminf returned
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), kLevels);
+    uint32_t words[2 * BITS];  // 64 codes
+#pragma unroll
+    for (int w = 0; w < 2 * BITS; ++w) words[w] = 0u;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float q = 0.f;
+      if (scale > 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[i], mn), scale)), 0.f), kLevels);
+      words[i / (32 / BITS)] |= (uint32_t)q << (BITS * (i % (32 / BITS)));
+    }
+    const int64_t u = unit_of(s, l, b, h);
+    unsigned char* rec = pool + (u * s.Nmax + t0 + t) * Q::kBytes;
+    uint4* codes = reinterpret_cast<uint4*>(rec + (size_t)(kv * NG + g) * 64 * BITS / 8);
+#pragma unroll
+    for (int v = 0; v < BITS / 2; ++v)
+      codes[v] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
+    *reinterpret_cast<float2*>(rec + Q::kParamOff + 8 * (kv * NG + g)) = make_float2(scale, mn);
+    const int p = s.persist_slot[l * s.Hkv + h];
+    if (p >= 0 && s.resident != nullptr) {
+      const int64_t ru = ((int64_t)l * s.B + b) * s.P + p;
+      uint4* dst = reinterpret_cast<uint4*>(s.resident + (ru * s.Nmax + t0 + t) * 2 * D + kv * D + 64 * g);
+#pragma unroll
+      for (int v = 0; v < BITS / 2; ++v)
+        dequant_vec<BITS>(make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]), scale, mn,
+                          dst + v * (16 / BITS));
+    }
+  }
+}
+
+template <int D, int BITS>
+cudaError_t launch_pool_write_q(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
+                                const uint16_t* vdev, cudaStream_t st) {
+  const int64_t total = n * s.Hkv * 2 * (D / 64);
+  const int64_t blocks = (total + 127) / 128;
+  k_pool_write_q<D, BITS><<<(unsigned)(blocks < 152 * 32 ? blocks : 152 * 32), 128, 0, st>>>(s, l, b, t0, n, kdev,
+                                                                                            vdev);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
@@ -116,6 +192,12 @@ cudaError_t launch_hash_keys(const DevState& s, int l, int b, int64_t t0, int64_
 cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
                               const uint16_t* vdev, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
+  if (s.kv_bits != 16) {
+    if (s.d == 128) return s.kv_bits == 4 ? launch_pool_write_q<128, 4>(s, l, b, t0, n, kdev, vdev, st)
+                                           : launch_pool_write_q<128, 2>(s, l, b, t0, n, kdev, vdev, st);
+    return s.kv_bits == 4 ? launch_pool_write_q<64, 4>(s, l, b, t0, n, kdev, vdev, st)
+                          : launch_pool_write_q<64, 2>(s, l, b, t0, n, kdev, vdev, st);
+  }
   const int64_t total = n * s.Hkv * 2 * (s.d / 8);
   const int64_t blocks = (total + 255) / 256;
   k_pool_write<<<(unsigned)(blocks < 152 * 32 ? blocks : 152 * 32), 256, 0, st>>>(s, l, b, t0, n, kdev, vdev);

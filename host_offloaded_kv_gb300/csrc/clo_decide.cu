@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
       const int li = dec == CLO_DEC_HIT ? 0 : (dec == CLO_DEC_PERSIST ? 1 : 2);
       int32_t* lst = li == 0 ? s.hit_list : (li == 1 ? s.pers_list : s.miss_list);
       lst[(int64_t)l * BH + atomicAdd(&s.lcnt[li * s.L + l], 1)] = (int32_t)u;
-      const int64_t rec = 4LL * d;
-      const unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * rec) : 0ull;
+      const int64_t rec = 4LL * d;  // bf16 K|V row in HBM
+      const unsigned long long host = (dec == CLO_DEC_MISS) ? (unsigned long long)(k * s.rec_bytes) : 0ull;
       int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
       if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
       if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;

@@ -91,10 +91,19 @@ struct SelSmem {
   int misc[8];
 };
 
+// A whole unit of up to 32K tokens selected by one compute group.
+struct SelUnitSmem {
+  uint16_t scores[32768];
+  uint32_t hist[kNBPad];
+  int wc[kCompWarps][2];
+  int misc[8];
+};
+
 template <int D, int NBUF>
 union CompSmem {
   AttSmem<D, NBUF> att;
   SelSmem sel;
+  SelUnitSmem unit;
 };
 
 // ---- hash-code scores -------------------------------------------------------------------
@@ -381,6 +390,121 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
         const int pos = off + __popc(bsel & lt);
         if (pos < k)
           out[pos] = (int32_t)(t0 + t);
+        else
+          atomicOr(s.err, kErrBounds);
+      }
+      eqb += __popc(beq);
+      off += __popc(bsel);
+    }
+  }
+  comp_bar();  // the group's index writes happen before gtid 0's release
+  if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
+}
+
+// ---- selection item: a whole unit (contexts up to 32K tokens) ----------------------------
+// One compute group scores all of the unit's tokens into shared memory, finds the
+// threshold T from its histogram and compacts: no hand-off with other groups.
+template <int G>
+__device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid) {
+  constexpr int NB = 128 * G + 1;
+  constexpr int kU = 4;  // code loads in flight per lane (more would spill in this kernel)
+  const int b = (int)((u / s.Hkv) % s.B);
+  const int N = (int)s.ntok[b];
+  const int k = s.kcount[b];
+  const int warp = gtid >> 5, lane = gtid & 31;
+  const int WSEG = (((N + kCompWarps - 1) / kCompWarps) + 255) / 256 * 256;  // tokens per warp
+  for (int i = gtid; i < NB; i += kCompThreads) sm.hist[i] = 0;
+  QPlanes<G> qp;
+  load_qplanes<G>(s, u, qp);
+  comp_bar();
+  const int w0 = warp * WSEG;
+  const int w1 = (w0 + WSEG < N) ? w0 + WSEG : N;
+  const uint4* src = s.codes + u * s.Nmax;
+  for (int base = w0; base < w1; base += 32 * kU) {
+    uint4 cv[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int t = base + 32 * j + lane;
+      if (t < w1) cv[j] = ld_nc_v4(src + t);
+    }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int t = base + 32 * j + lane;
+      if (t < w1) {
+        const int sc = score_of<G>(cv[j], qp);
+        sm.scores[t] = (uint16_t)sc;
+        atomicAdd(&sm.hist[sc], 1u);
+      }
+    }
+  }
+  comp_bar();
+  if (warp == 0) {  // threshold T: largest score with count(score >= T) >= k
+    const int seg = (NB + 31) / 32;
+    const int hi = NB - lane * seg;
+    const int lo = hi - seg > 0 ? hi - seg : 0;
+    int segsum = 0;
+    for (int bin = lo; bin < hi; ++bin) segsum += (int)sm.hist[bin];
+    int incl = segsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - segsum;
+    if (excl < k && incl >= k) {
+      int run = excl;
+      for (int bin = hi - 1; bin >= lo; --bin) {
+        if (run + (int)sm.hist[bin] >= k) {
+          sm.misc[0] = bin;
+          sm.misc[1] = run;
+          break;
+        }
+        run += (int)sm.hist[bin];
+      }
+    }
+  }
+  comp_bar();
+  const int T = sm.misc[0];
+  const int take_eq = k - sm.misc[1];  // ties taken, lowest index first
+  {
+    int gt = 0, eq = 0;
+    for (int t = w0 + lane; t < w1; t += 32) {
+      const int sc = sm.scores[t];
+      gt += sc > T;
+      eq += sc == T;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o);
+    }
+    if (lane == 0) {
+      sm.wc[warp][0] = gt;
+      sm.wc[warp][1] = eq;
+    }
+  }
+  comp_bar();
+  int off = 0, eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    int tk = take_eq - eqb;
+    tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);
+    off += sm.wc[w][0] + tk;
+    eqb += sm.wc[w][1];
+  }
+  {
+    const uint32_t lt = (1u << lane) - 1u;
+    int32_t* out = s.idx + u * s.kmax;
+    for (int base = w0; base < w1; base += 32) {
+      const int t = base + lane;
+      const int sc = t < w1 ? (int)sm.scores[t] : -1;
+      const bool is_eq = sc == T;
+      const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
+      const bool sel = sc > T || (is_eq && eqb + __popc(beq & lt) < take_eq);
+      const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
+      if (sel) {
+        const int pos = off + __popc(bsel & lt);
+        if (pos < k)
+          out[pos] = t;
         else
           atomicOr(s.err, kErrBounds);
       }
@@ -682,10 +806,72 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
 // indices are checked and staged in shared memory first, so every round trip to host
 // memory is a single dependent load; each round keeps kFetchUnroll 16-byte loads per
 // lane in flight (with d = 128 one warp-wide load is one whole 512-byte K|V record).
+// bf16 records: K|V rows copied as they are (16-byte loads, one record per warp-wide load).
+template <int D, int FU>
+__device__ __forceinline__ void copy_rows(const DevState& s, int64_t u, int64_t r0, int nr, const int32_t* sidx,
+                                          int lane) {
+  constexpr int VPR = D / 4;  // 16-byte vectors per K|V record
+  const uint4* pool = reinterpret_cast<const uint4*>(s.pool) + u * s.Nmax * VPR;
+  uint4* slot = reinterpret_cast<uint4*>(s.slots) + (u * s.kmax + r0) * VPR;
+  const int total = nr * VPR;
+  for (int e0 = lane; e0 < total; e0 += 32 * FU) {
+    uint4 v[FU];
+#pragma unroll
+    for (int j = 0; j < FU; ++j) {
+      const int e = e0 + 32 * j;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (e < total) {
+        const int t = sidx[e / VPR];
+        if (t >= 0) v[j] = ld_nc_v4(pool + (int64_t)t * VPR + (e % VPR));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < FU; ++j) {
+      const int e = e0 + 32 * j;
+      if (e < total) slot[e] = v[j];
+    }
+  }
+}
+
+// Quantised records: lane (row slot, code vector j) loads one 16-byte code vector and
+// its group's (scale, min), and writes the dequantised bf16 values to the slot row.
+template <int D, int FU, int BITS>
+__device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_t r0, int nr, const int32_t* sidx,
+                                            int lane) {
+  using Q = QRec<D, BITS>;
+  constexpr int PV = Q::kCodeVecs;  // lanes per row
+  constexpr int RPI = 32 / PV;      // rows per warp-wide round
+  const unsigned char* pool = reinterpret_cast<const unsigned char*>(s.pool) + u * s.Nmax * Q::kBytes;
+  uint4* slot = reinterpret_cast<uint4*>(s.slots) + (u * s.kmax + r0) * (D / 4);
+  const int rl = lane / PV, j = lane % PV, gi = j / Q::kVecsPerGroup;
+  for (int rb = 0; rb < nr; rb += RPI * FU) {
+    uint4 cv[FU];
+    float2 pp[FU];
+#pragma unroll
+    for (int f = 0; f < FU; ++f) {
+      const int r = rb + f * RPI + rl;
+      cv[f] = make_uint4(0, 0, 0, 0);
+      pp[f] = make_float2(0.f, 0.f);
+      if (r < nr) {
+        const int t = sidx[r];
+        if (t >= 0) {
+          const unsigned char* rec = pool + (int64_t)t * Q::kBytes;
+          cv[f] = ld_nc_v4(reinterpret_cast<const uint4*>(rec) + j);
+          pp[f] = ld_nc_f2(rec + Q::kParamOff + 8 * gi);
+        }
+      }
+    }
+#pragma unroll
+    for (int f = 0; f < FU; ++f) {
+      const int r = rb + f * RPI + rl;
+      if (r < nr) dequant_vec<BITS>(cv[f], pp[f].x, pp[f].y, slot + (int64_t)r * (D / 4) + j * Q::kOutVecs);
+    }
+  }
+}
+
 template <int D, int FU>
 __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int lane, int32_t* sidx) {
   constexpr int kFetchUnroll = FU;
-  constexpr int VPR = D / 4;  // 16-byte vectors per K|V record
   const int NS = s.nchunk, RS = kChunkRows, L = s.L, BH = s.B * s.Hkv;
   const int64_t n_items = (int64_t)n_miss * NS;
   while (true) {
@@ -722,26 +908,12 @@ __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int 
         sidx[i] = t;
       }
       __syncwarp();
-      const uint4* pool = reinterpret_cast<const uint4*>(s.pool) + u * s.Nmax * VPR;
-      uint4* slot = reinterpret_cast<uint4*>(s.slots) + (u * s.kmax + r0) * VPR;
-      const int total = nr * VPR;
-      for (int e0 = lane; e0 < total; e0 += 32 * kFetchUnroll) {
-        uint4 v[kFetchUnroll];
-#pragma unroll
-        for (int j = 0; j < kFetchUnroll; ++j) {
-          const int e = e0 + 32 * j;
-          v[j] = make_uint4(0, 0, 0, 0);
-          if (e < total) {
-            const int t = sidx[e / VPR];
-            if (t >= 0) v[j] = ld_nc_v4(pool + (int64_t)t * VPR + (e % VPR));
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kFetchUnroll; ++j) {
-          const int e = e0 + 32 * j;
-          if (e < total) slot[e] = v[j];
-        }
-      }
+      if (s.kv_bits == 16)
+        copy_rows<D, kFetchUnroll>(s, u, r0, nr, sidx, lane);
+      else if (s.kv_bits == 4)
+        copy_rows_q<D, kFetchUnroll, 4>(s, u, r0, nr, sidx, lane);
+      else
+        copy_rows_q<D, kFetchUnroll, 2>(s, u, r0, nr, sidx, lane);
     }
     __threadfence();
     __syncwarp();  // also: sidx is rewritten by the next item
@@ -760,7 +932,7 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
   __shared__ int pre[3][kMaxLayers + 1];  // hit, persistent, missed lists
   __shared__ long long sec_start[6];
   __shared__ int s_item;
-  __shared__ unsigned long long s_t0;  // start of the group's item (timing mode)
+  __shared__ unsigned long long s_t0, s_t1;  // start of the group's item, end of its waits (timing mode)
   __shared__ int32_t fidx[FW][kChunkRows];
   extern __shared__ __align__(128) unsigned char dsm[];
   Smem& sm = *reinterpret_cast<Smem*>(dsm);
@@ -822,7 +994,10 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
       const int p = (int)(j / NC), c = (int)(j % NC);
       const int l = layer_of(pl, L, p);
       const int64_t u = lst[(int64_t)l * BH + (p - pl[l])];
-      sel_chunk<G>(s, sm.sel, u, c, gtid);
+      if (NC == 1 && s.sel_chunk >= s.Nmax)
+        sel_unit<G>(s, sm.unit, u, gtid);
+      else
+        sel_chunk<G>(s, sm.sel, u, c, gtid);
       if (s.timeline && gtid == 0) {
         const uint64_t t1 = global_timer_ns();
         atomicMax(&s.timeline[sec == 0 ? TL_SEL_MISS_END : TL_SEL_PERS_END], t1);
@@ -848,11 +1023,13 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
         }
         comp_bar();
       }
+      if (s.timeline && gtid == 0) s_t1 = global_timer_ns();
       attend_split<D, NBUF>(s, sm.att, q, out, u, c, gtid);
       if (s.timeline && gtid == 0) {
         const uint64_t t1 = global_timer_ns();
         atomicMax(&s.timeline[TL_COMP_END], t1);
         atomicAdd(&s.timeline[TL_ATT_SUM_NS], t1 - s_t0);
+        atomicAdd(&s.timeline[TL_ATT_RUN_NS], t1 - s_t1);
         atomicAdd(&s.timeline[TL_ATT_ITEMS], 1ull);
       }
     }
@@ -905,6 +1082,22 @@ cudaError_t launch_d(const DevState& s, const uint16_t* q, float* out, cudaStrea
   }
 }
 
+// Dequantises the records of tokens [t0, t1) of unit u into bf16 rows at dst.
+template <int D, int BITS>
+__device__ __forceinline__ void fill_q(const DevState& s, int64_t u, int64_t t0, int64_t t1, uint4* dst) {
+  using Q = QRec<D, BITS>;
+  const unsigned char* pool = reinterpret_cast<const unsigned char*>(s.pool) + (u * s.Nmax + t0) * Q::kBytes;
+  const int64_t n = (t1 - t0) * Q::kCodeVecs;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = e / Q::kCodeVecs;
+    const int j = (int)(e % Q::kCodeVecs);
+    const unsigned char* rec = pool + t * Q::kBytes;
+    const float2 pp = ld_nc_f2(rec + Q::kParamOff + 8 * (j / Q::kVecsPerGroup));
+    dequant_vec<BITS>(ld_nc_v4(reinterpret_cast<const uint4*>(rec) + j), pp.x, pp.y,
+                      dst + t * (D / 4) + j * Q::kOutVecs);
+  }
+}
+
 // Full K/V of persistent heads, host pool -> resident HBM copy, tokens [t0, t1).
 __global__ void k_resident_fill(DevState s, int64_t t0, int64_t t1) {
   const int vpr = s.d / 4;
@@ -917,9 +1110,16 @@ __global__ void k_resident_fill(DevState s, int64_t t0, int64_t t1) {
     if (p < 0) continue;
     const int64_t tend = (t1 < s.ntok[b]) ? t1 : s.ntok[b];
     if (tend <= t0) continue;
+    uint4* dst = reinterpret_cast<uint4*>(s.resident) + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax + t0) * vpr;
+    if (s.kv_bits != 16) {  // quantised pool: dequantise every code vector
+      if (s.d == 128)
+        s.kv_bits == 4 ? fill_q<128, 4>(s, u, t0, tend, dst) : fill_q<128, 2>(s, u, t0, tend, dst);
+      else
+        s.kv_bits == 4 ? fill_q<64, 4>(s, u, t0, tend, dst) : fill_q<64, 2>(s, u, t0, tend, dst);
+      continue;
+    }
     const int64_t n = (tend - t0) * vpr;
     const uint4* src = reinterpret_cast<const uint4*>(s.pool) + (u * s.Nmax + t0) * vpr;
-    uint4* dst = reinterpret_cast<uint4*>(s.resident) + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax + t0) * vpr;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x)
       dst[e] = ld_nc_v4(src + e);
   }

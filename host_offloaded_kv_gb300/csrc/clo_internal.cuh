@@ -11,6 +11,7 @@
 //   resident   (HBM)                   bf16 [L][B][P][Nmax][K | V]   persistent heads' full K/V
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -98,6 +99,8 @@ struct DevState {
   int adapt_active;             // this launch updates s_hat and tau from cos_sum
   double tau_ema;               // weight of the newest step in the s_hat average
   float tau_offset;             // tau = s_hat - tau_offset
+  int kv_bits;                  // host pool storage: 16 (bf16), 4 or 2
+  int rec_bytes;                // bytes of one token's K|V record in the host pool
   int l0, l1;                   // layers of this launch: [l0, l1)
   int q_l0;                     // layer of the first [B][Hq][d] block of the q / out buffers
 };
@@ -121,6 +124,7 @@ enum Timeline : int {
   TL_ATT_ITEMS = 12,     // attention splits run
   TL_DEC_START = 13,     // a CTA of the decide kernel started (first writer)
   TL_DEC_END = 14,       // last CTA of the decide kernel finished
+  TL_ATT_RUN_NS = 15,    // summed durations of attention splits after their waits
   kTimelineSlots = 16
 };
 constexpr int kSelChunkMax = 16384;  // tokens per selection chunk, at most (8192 or 16384)
@@ -223,6 +227,47 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float2 ld_nc_f2(const void* p) {
+  float2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
+// ---- quantised host records ---------------------------------------------------------------
+// Record of one token and kv head: [K codes | V codes | (scale, min) fp32 per 64-channel
+// group, K groups then V groups]; value i of a row sits in 32-bit word i / (32 / BITS)
+// at bit BITS * (i % (32 / BITS)).  One 16-byte code vector holds 128 / BITS values of
+// one group.
+template <int D, int BITS>
+struct QRec {
+  static constexpr int kCodeVecs = 2 * D * BITS / 128;  // 16-byte code vectors per record
+  static constexpr int kVecsPerGroup = BITS / 2;          // 64 values per group
+  static constexpr int kOutVecs = 16 / BITS;              // bf16 uint4 per code vector
+  static constexpr int kParamOff = kCodeVecs * 16;
+  static constexpr int kBytes = kParamOff + (2 * D / 64) * 8;
+};
+
+// Dequantises one 16-byte code vector: value = bf16(fma(q, scale, mn)).
+template <int BITS>
+__device__ __forceinline__ void dequant_vec(const uint4 p, float scale, float mn, uint4* out) {
+  constexpr int PER = 32 / BITS;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+  uint32_t o[2 * PER];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < PER; j += 2) {
+      const float a = fmaf((float)((w[i] >> (BITS * j)) & MASK), scale, mn);
+      const float b = fmaf((float)((w[i] >> (BITS * (j + 1))) & MASK), scale, mn);
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+      o[(i * PER + j) / 2] = lo | (hi << 16);
+    }
+#pragma unroll
+  for (int v = 0; v < PER / 2; ++v) out[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -107,6 +107,15 @@ typedef struct clo_config {
    * from the next step.  Persistent heads stay as chosen.  0 = off (default). */
   int32_t adaptive_tau;
   double tau_ema;          /* weight of the newest step, in (0, 1]; default 1/16 */
+  /* storage of the host pool ([KVO] section on quantised offloading: low-bit KV
+   * crosses the link and is dequantised on the GPU): 16 (bf16, default; 0 means
+   * 16), 4 or 2 bits per value.  Quantised records: per token and per K or V row,
+   * groups of 64 channels, each with an fp32 scale = (max - min) / (2^bits - 1) and
+   * fp32 min (+0 for a zero minimum); code q = clamp(rint((x - min) / scale), 0, 2^bits - 1) (0 if scale
+   * is 0); the GPU sees bf16(fma(q, scale, min)) in the cache slots and resident
+   * copies.  Key hash codes come from the keys as appended.  Record bytes per token
+   * and kv head: 4 d (bf16), d + d/4 (4 bits), d/2 + d/4 (2 bits). */
+  int32_t kv_bits;
 } clo_config;
 
 typedef struct clo_stats_t {
@@ -213,7 +222,8 @@ CLO_API const char* clo_last_error(void);
  *                       [8] summed attention waits on fetch flags, [9] summed durations
  *                       of selection chunks, [10] their number, [11] summed durations
  *                       of attention splits, [12] their number, [13] first CTA of
- *                       the step's decide kernel started, [14] its last CTA finished
+ *                       the step's decide kernel started, [14] its last CTA finished,
+ *                       [15] summed durations of attention splits after their waits
  * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,

@@ -8,6 +8,8 @@ from .clo_oracle import (  # noqa: F401
     OracleCLO,
     load_oracle,
     kv_bytes_per_token,
+    kv_roundtrip,
+    kv_record_bytes,
     hash_codes,
     cosine,
     scores,

@@ -230,3 +230,59 @@ int orc_num_threads(void) {
   }
   return n;
 }
+
+/* Quantised host KV ([KVO] section on quantised offloading: the offloaded K/V are
+ * stored at a few bits per value with an asymmetric scale and offset and
+ * dequantised on the GPU after the transfer).  Reading used here, per token and
+ * per K or V row, in groups of 64 consecutive channels, every operation in fp32
+ * rounded to nearest even:
+ *   mn = min of the group (+0 for a zero), mx = max, scale = (mx - mn) / (2^bits - 1),
+ *   q_i = 0 if scale == 0, else clamp(rint((x_i - mn) / scale), 0, 2^bits - 1),
+ *   value_i = bf16(fma(q_i, scale, mn)).
+ * orc_kv_roundtrip maps n_values bf16 values (a whole number of groups) to the
+ * values the GPU sees after dequantisation. */
+static float bf16_to_float(uint16_t b) {
+  uint32_t bits = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &bits, 4);
+  return f;
+}
+
+static uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u); /* NaN stays NaN */
+  const uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+void orc_kv_roundtrip(const uint16_t* x, int64_t n_values, int bits, uint16_t* y) {
+  const float levels = (float)((1 << bits) - 1);
+  for (int64_t g0 = 0; g0 < n_values; g0 += 64) {
+    float mn = bf16_to_float(x[g0]), mx = mn;
+    for (int i = 1; i < 64; ++i) {
+      const float v = bf16_to_float(x[g0 + i]);
+      if (v < mn) mn = v;
+      if (v > mx) mx = v;
+    }
+    mn = mn + 0.0f; /* a zero minimum is +0 whichever zero the comparison kept */
+    const float scale = (mx - mn) / levels;
+    for (int i = 0; i < 64; ++i) {
+      float q = 0.0f;
+      if (scale > 0.0f) {
+        q = rintf((bf16_to_float(x[g0 + i]) - mn) / scale);
+        if (q < 0.0f) q = 0.0f;
+        if (q > levels) q = levels;
+      }
+      y[g0 + i] = float_to_bf16_rne(fmaf(q, scale, mn));
+    }
+  }
+}
+
+/* Bytes of one token's quantised K|V record of one kv head: the codes of both
+ * rows and an (fp32 scale, fp32 min) pair per group; 4 d bytes (bf16) for bits 16. */
+int64_t orc_kv_record_bytes(int64_t d, int bits) {
+  if (bits >= 16) return 4 * d;
+  return 2 * d * bits / 8 + (2 * d / 64) * 8;
+}

@@ -74,6 +74,10 @@ def load_oracle():
     lib.orc_attention.argtypes = [_p, _int, _int, _p, _p, _i64, _p]
     lib.orc_num_threads.restype = _int
     lib.orc_num_threads.argtypes = []
+    lib.orc_kv_roundtrip.restype = None
+    lib.orc_kv_roundtrip.argtypes = [_p, _i64, _int, _p]
+    lib.orc_kv_record_bytes.restype = _i64
+    lib.orc_kv_record_bytes.argtypes = [_i64, _int]
     _lib = lib
     return lib
 
@@ -109,6 +113,23 @@ def cosine(a: np.ndarray, b: np.ndarray) -> float:
     b = _c(b, np.uint16).reshape(-1)
     assert a.size == b.size
     return float(load_oracle().orc_cosine(a.ctypes.data, b.ctypes.data, a.size))
+
+
+def kv_roundtrip(x: np.ndarray, bits: int) -> np.ndarray:
+    """bf16 values (last axis a multiple of 64) -> their values after the host pool's
+    b-bit quantisation and the GPU's dequantisation (identity for bits 16)."""
+    x = _c(x, np.uint16)
+    if bits >= 16:
+        return x.copy()
+    assert x.shape[-1] % 64 == 0
+    y = np.empty_like(x)
+    load_oracle().orc_kv_roundtrip(x.ctypes.data, x.size, int(bits), y.ctypes.data)
+    return y
+
+
+def kv_record_bytes(d: int, bits: int) -> int:
+    """Host-pool bytes of one token's K|V record of one kv head."""
+    return int(load_oracle().orc_kv_record_bytes(int(d), int(bits)))
 
 
 def scores(qcodes: np.ndarray, kcodes: np.ndarray) -> np.ndarray:
@@ -171,13 +192,16 @@ class OracleCLO:
     units (they need only the queries)."""
 
     def __init__(self, L, B, Hq, Hkv, d, R, *, topk=0, topk_ratio=0.1, tau=None, persist_mask=None,
-                 warmup_steps=16, tau_offset=0.05, n_persist=0, ntok=None, adaptive_tau=False, tau_ema=0.0625):
+                 warmup_steps=16, tau_offset=0.05, n_persist=0, ntok=None, adaptive_tau=False, tau_ema=0.0625,
+                 kv_bits=16):
         load_oracle()
         assert Hq % Hkv == 0
         self.L, self.B, self.Hq, self.Hkv, self.d = L, B, Hq, Hkv, d
         self.G = Hq // Hkv
         self.R = _c(R, np.uint16).reshape(L, Hkv, d, 128)
         self.topk_fixed, self.ratio = int(topk), float(topk_ratio)
+        self.kv_bits = int(kv_bits)
+        self.record_bytes = kv_record_bytes(d, self.kv_bits)
         self.ntok = np.zeros(B, dtype=np.int64) if ntok is None else np.asarray(ntok, dtype=np.int64).copy()
         self.kv = {}
         self.kcodes = {}
@@ -215,8 +239,9 @@ class OracleCLO:
         K = _c(K, np.uint16)
         V = _c(V, np.uint16)
         assert K.shape == V.shape and K.shape[1] == self.d
-        self.kv[(l, b, h)] = (K, V)
+        # codes from the keys as given; attention sees the rows as stored in the pool
         self.kcodes[(l, b, h)] = hash_codes(K, self.R[l, h])
+        self.kv[(l, b, h)] = (kv_roundtrip(K, self.kv_bits), kv_roundtrip(V, self.kv_bits))
         self.ntok[b] = K.shape[0]
 
     def k_of(self, b: int) -> int:
@@ -263,7 +288,7 @@ class OracleCLO:
             for b in range(B):
                 for h in range(Hkv):
                     if dec[l, b, h] == DEC_MISS:
-                        host += self.k_of(b) * 4 * d
+                        host += self.k_of(b) * self.record_bytes
         res.host_bytes = host
         qr = q.reshape(L, B, Hkv, G, d)
         for (l, b, h), (K, V) in self.kv.items():

@@ -42,6 +42,7 @@ class Spec:
     kv_override: dict = field(default_factory=dict)  # (l, b) -> (K, V) replacing generated data
     adaptive_tau: bool = False
     tau_ema: float = 0.0625
+    kv_bits: int = 16
 
 
 class LockStep:
@@ -59,11 +60,12 @@ class LockStep:
         self.lib = CLOContext(n_layers=s.L, batch=s.B, n_q_heads=s.Hq, n_kv_heads=s.Hkv, head_dim=s.d,
                               max_tokens=maxtok, hash_R=self.R, topk=s.topk, topk_ratio=s.topk_ratio, tau=tau,
                               persist_mask=s.persist_mask, warmup_steps=s.warmup_steps, tau_offset=s.tau_offset,
-                              n_persist=s.n_persist, adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema)
+                              n_persist=s.n_persist, adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema,
+                              kv_bits=s.kv_bits)
         self.orc = orc.OracleCLO(s.L, s.B, s.Hq, s.Hkv, s.d, self.R, topk=s.topk, topk_ratio=s.topk_ratio,
                                  tau=tau, persist_mask=s.persist_mask, warmup_steps=s.warmup_steps,
                                  tau_offset=s.tau_offset, n_persist=s.n_persist, ntok=s.ntok,
-                                 adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema)
+                                 adaptive_tau=s.adaptive_tau, tau_ema=s.tau_ema, kv_bits=s.kv_bits)
         units = s.sample if s.sample is not None else [
             (l, b, h) for l in range(s.L) for b in range(s.B) for h in range(s.Hkv)]
         self.units = list(units)
@@ -146,7 +148,7 @@ class LockStep:
             else:
                 assert np.array_equal(idx_lib, self.prev_idx[u]), f"unit {u}: hit changed the selection"
             if du == orc.DEC_MISS:
-                K, V = self.kv[u]
+                K, V = self.orc.kv[u]   # the rows as the pool stores them (dequantised if quantised)
                 rows = self.lib.slot_rows(*u)
                 assert np.array_equal(rows[:, 0, :], K[res.idx[u]]), f"unit {u}: gathered K rows differ"
                 assert np.array_equal(rows[:, 1, :], V[res.idx[u]]), f"unit {u}: gathered V rows differ"

@@ -416,3 +416,56 @@ def test_adaptive_tau_closed_form_converges_to_one():
     # with tau near 1 - 0.05 every reused head now hits (cos = 1 >= tau)
     r = o.step(q)
     assert np.all(r.decision == orc.DEC_HIT)
+
+
+# ---- quantised host KV -----------------------------------------------------------------
+def test_kv_record_bytes_worked_values():
+    # one token's K|V record of one kv head: codes of 2 d values at b bits plus one
+    # (fp32 scale, fp32 min) pair per 64-channel group; d = 128: 2*128*4/8 = 128 B of
+    # codes + 4 groups * 8 B = 160 B at 4 bits, 64 + 32 = 96 B at 2 bits; bf16: 512 B
+    assert orc.kv_record_bytes(128, 4) == 160
+    assert orc.kv_record_bytes(128, 2) == 96
+    assert orc.kv_record_bytes(64, 4) == 80
+    assert orc.kv_record_bytes(64, 2) == 48
+    assert orc.kv_record_bytes(128, 16) == 512
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_kv_quant_grid_values_roundtrip_exactly(bits):
+    # values on the quantisation grid (offset and power-of-two step exact in fp32) come back unchanged
+    rng = np.random.default_rng(3)
+    levels = (1 << bits) - 1
+    for step in (2.0 ** -3, 0.5, 4.0):
+        base = float(rng.integers(-8, 8)) * step
+        codes = rng.integers(0, levels + 1, size=(5, 64))
+        codes[:, 0], codes[:, 1] = 0, levels            # the group spans the whole grid
+        x = float_to_bf16(base + codes * step)
+        assert np.array_equal(bf16_to_float(x), base + codes * step)
+        assert np.array_equal(orc.kv_roundtrip(x, bits), x)
+
+
+def test_kv_quant_constant_group_is_exact():
+    x = np.full((3, 128), 0x3fc0, dtype=np.uint16)     # 1.5 everywhere: scale 0
+    for bits in (4, 2):
+        assert np.array_equal(orc.kv_roundtrip(x, bits), x)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_kv_quant_picks_the_nearest_level(bits):
+    # brute force over the 2^b levels of each group: the dequantised value is the level
+    # nearest to x (up to the rounding of the division), and the group minimum is exact
+    rng = np.random.default_rng(5 + bits)
+    x = float_to_bf16(rng.standard_normal((40, 64)) * rng.uniform(0.1, 5.0, size=(40, 1)))
+    y = bf16_to_float(orc.kv_roundtrip(x, bits)).astype(np.float64)
+    xf = bf16_to_float(x).astype(np.float64)
+    levels = (1 << bits) - 1
+    for g in range(x.shape[0]):
+        mn, mx = xf[g].min(), xf[g].max()
+        scale = float(np.float32(np.float32(mx - mn) / np.float32(levels)))
+        grid = mn + np.arange(levels + 1) * scale
+        for i in range(64):
+            dist = np.abs(xf[g, i] - grid)
+            q = int(np.argmin(np.abs(y[g, i] - grid)))   # level the value came from
+            assert dist[q] <= dist.min() + 1e-6 * scale
+            assert abs(y[g, i] - grid[q]) <= abs(grid[q]) * 2.0 ** -8 + 1e-30
+        assert y[g][np.argmin(xf[g])] == mn
