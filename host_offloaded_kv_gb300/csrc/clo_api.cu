@@ -60,6 +60,7 @@ struct clo_ctx {
   int64_t step = 0;
   bool warmup_mode = false;
   int kv_bits = 16;
+  int whole_unit_min_units = 0;  // launches with at least this many units select units whole
   int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
   int W = 0;
   bool warmup_done = false;
@@ -246,6 +247,12 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   // scores fit in its shared memory); longer ones in chunks of 16384 tokens by several
   s.sel_chunk = c->Nmax <= 32768 ? (int)c->Nmax : kSelChunkMax;
   s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
+  {  // launches with few units split them into 8192-token chunks (see enqueue_layers)
+    int sms = 0;
+    CLO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    c->whole_unit_min_units = 4 * sms;
+  }
+  const int nch_max = (int)((c->Nmax + 8191) / 8192);
   s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
   {
     size_t off = 2 * (size_t)C_NUM * kCtrLanes;
@@ -292,7 +299,7 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.cos_sum = nullptr;
     s.cos_cnt = nullptr;
   }
-  CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * s.nch));
+  CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * nch_max));
   CLO_TRY(c->dalloc(&s.sel_thr, (size_t)U));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
   CLO_TRY(c->dalloc(&s.err, 1));
@@ -428,6 +435,14 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   s.l0 = l0;
   s.l1 = l1;
   s.q_l0 = l0;
+  // selection granularity: a context of up to 32K tokens is selected whole by one compute
+  // group when the launch has units enough to occupy the groups; otherwise (one layer
+  // of a layer-by-layer step, small batches) in chunks of 8192 tokens by several
+  // groups, which selects each unit sooner
+  const int64_t units = (int64_t)(l1 - l0) * c->B * c->Hkv;
+  if (c->Nmax <= 32768)
+    s.sel_chunk = units >= c->whole_unit_min_units ? (int)c->Nmax : 8192;
+  s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
   const bool warm = c->warmup_mode && c->step < c->W;
   s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
   const bool timed = c->cfg.timing != 0;

@@ -110,3 +110,12 @@ def test_hash_cancellations_take_the_exact_tiers():
         ls.step()
     finally:
         ls.close()
+
+
+def test_whole_unit_selection_many_units():
+    # 2 layers x 38 sequences x 8 kv heads = 608 units: enough to select each unit whole
+    # with one compute group (the per-chunk path is covered by the smaller cases above);
+    # ragged lengths, G = 4
+    ntok = [3000 - 37 * b for b in range(38)]
+    spec = Spec(L=2, B=38, Hq=32, Hkv=8, d=64, ntok=ntok, seed=61, tau=0.9, rho=(0.8, 0.99))
+    _run(spec, 3)
