@@ -54,6 +54,8 @@ def parse_args():
                    help="online adaptive thresholds after warm-up (running average of the live cosines)")
     p.add_argument("--kv-bits", type=int, default=16, choices=[16, 4, 2],
                    help="host pool storage: bf16, or 4/2-bit asymmetric codes dequantised on the GPU")
+    p.add_argument("--grow", action="store_true",
+                   help="streaming growth: every step first appends one token per (layer, sequence)")
     p.add_argument("--layerwise", action="store_true",
                    help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -238,7 +240,10 @@ def run_gb300(args, rank, world, local_rank):
     w = workload_from_args(args)
     L, B, Hq, Hkv, d, N = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_tokens
     rec_bytes = 4 * d if args.kv_bits == 16 else 2 * d * args.kv_bits // 8 + (2 * d // 64) * 8
-    pool_bytes = L * B * Hkv * N * rec_bytes
+    K, W = args.steps, args.warmup
+    n_grow = (w.warmup_steps if w.tau_fixed is None else 0) + W + 2 * K + 1 if args.grow else 0
+    Ncap = N + n_grow                       # growth appends one token per step
+    pool_bytes = L * B * Hkv * Ncap * rec_bytes
     if mem_available_bytes() < pool_bytes * 1.15 + (1 << 30):
         raise SystemExit(f"not enough host memory for the {pool_bytes / 2**30:.1f} GiB pinned pool of {w.name}")
     torch.cuda.set_device(local_rank)
@@ -248,17 +253,27 @@ def run_gb300(args, rank, world, local_rank):
     R = syn.hash_matrices(L, Hkv, d)
     tau = None if w.tau_fixed is None else np.full(L * Hkv, w.tau_fixed, dtype=np.float32)
     t0 = time.time()
-    lib = CLOContext(n_layers=L, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, max_tokens=N, hash_R=R,
+    lib = CLOContext(n_layers=L, batch=B, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, max_tokens=Ncap, hash_R=R,
                      topk=w.topk, topk_ratio=w.topk_ratio, tau=tau, warmup_steps=w.warmup_steps,
                      tau_offset=w.tau_offset, n_persist=w.n_persist if tau is None else 0, timing=True,
                      stream=stream.cuda_stream, adaptive_tau=args.adaptive_tau, kv_bits=args.kv_bits)
     if args.layerwise:
-        def step_fn(q, o, io_on_device=None):
+        def decode(q, o, io_on_device=None):
             for l in range(L):
                 lib.decode_layer(l, q[l], o[l], io_on_device)
     else:
-        def step_fn(q, o, io_on_device=None):
+        def decode(q, o, io_on_device=None):
             lib.decode_step(q, o, io_on_device)
+    grow_src = {"dev": None, "host": None, "i": 0}
+
+    def step_fn(q, o, io_on_device=None):
+        if args.grow:   # one new token per (layer, sequence), then the step over the grown context
+            src = grow_src["dev"] if io_on_device is None else grow_src["host"]
+            i = grow_src["i"]
+            lib.append_step(src[0][i % src[0].shape[0]], src[1][i % src[1].shape[0]],
+                            None if io_on_device is None else io_on_device)
+            grow_src["i"] = i + 1
+        decode(q, o, io_on_device)
     Kbuf = np.empty((N, Hkv, d), dtype=np.uint16)
     Vbuf = np.empty((N, Hkv, d), dtype=np.uint16)
     for l in range(L):
@@ -268,9 +283,18 @@ def run_gb300(args, rank, world, local_rank):
     t_setup = time.time() - t0
     del Kbuf, Vbuf
 
+    if args.grow:   # the appended tokens' rows, from the generator at positions N, N+1, ...
+        kn = np.empty((n_grow, L, B, Hkv, d), dtype=np.uint16)
+        vn = np.empty_like(kn)
+        for i in range(n_grow):
+            for l in range(L):
+                for b in range(B):
+                    Kt, Vt = syn.layer_seq_kv(l, b, Hkv, N + i, 1, d)
+                    kn[i, l, b], vn[i, l, b] = Kt[0], Vt[0]
+        grow_src["dev"] = (torch.from_numpy(kn.view(np.int16)).to(dev), torch.from_numpy(vn.view(np.int16)).to(dev))
+        grow_src["host"] = (torch.from_numpy(kn.view(np.int16)).pin_memory(), torch.from_numpy(vn.view(np.int16)).pin_memory())
     qs = syn.query_stream(L, B, Hq, d, w.rho_lo, w.rho_hi)
     n_prof = w.warmup_steps if tau is None else 0
-    K, W = args.steps, args.warmup
     n_dev = n_prof + W + K
     qdev = torch.empty((n_dev, L, B, Hq, d), dtype=torch.int16, device=dev)
     qh = np.empty((L, B, Hq, d), dtype=np.uint16)
@@ -339,7 +363,8 @@ def run_gb300(args, rank, world, local_rank):
         lib.stats()
         sec = max_over_ranks(t2 - t1, world)
         e2e = {"value": whole_job_rate(B * (Ke - 1), sec, world), "unit": UNIT,
-               "h2d_bytes_per_step": L * B * Hq * d * 2, "d2h_bytes_per_step": L * B * Hq * d * 4}
+               "h2d_bytes_per_step": L * B * Hq * d * 2 + (2 * L * B * Hkv * d * 2 if args.grow else 0),
+               "d2h_bytes_per_step": L * B * Hq * d * 4}
 
     link_gbs = max(link_gbs_before, pinned_h2d_gbs(dev))
     lib.close()
@@ -387,8 +412,10 @@ def run_gb300(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1),
-                   "mode": "layer by layer (clo_decode_layer per layer)" if args.layerwise else "whole step"},
-        "gpu_launches": 2 * steps * (L if args.layerwise else 1),
+                   "mode": ("layer by layer (clo_decode_layer per layer)" if args.layerwise else "whole step")
+                   + (f", growing context: one token appended per step (clo_append_step), {N} -> {Ncap - 1} tokens"
+                      if args.grow else "")},
+        "gpu_launches": steps * (2 * (L if args.layerwise else 1) + (3 if args.grow else 0)),
         "roofline": roofline,
         "step_roofline": {"bound": "max(HBM alg bytes / HBM peak, host bytes / link peak)",
                           "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,

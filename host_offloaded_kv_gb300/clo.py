@@ -24,7 +24,8 @@ CLO_SET_DROP_FLAG_LAYER, CLO_SET_WAIT_TIMEOUT_NS = 1, 2
 _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ERR_CUDA", 4: "CLO_ERR_TIMEOUT",
                  5: "CLO_ERR_STATE", 6: "CLO_ERR_CAPACITY", 7: "CLO_ERR_DEVICE"}
 
-EXPORTED = ["clo_config_default", "clo_init", "clo_destroy", "clo_append_kv", "clo_decode_step", "clo_decode_layer",
+EXPORTED = ["clo_config_default", "clo_init", "clo_destroy", "clo_append_kv", "clo_append_step", "clo_decode_step",
+            "clo_decode_layer",
             "clo_sync", "clo_stats", "clo_last_error", "clo_debug_get", "clo_set", "clo_sparse_attention_noalloc"]
 
 
@@ -94,6 +95,8 @@ def load_library(path: str = LIB_PATH):
     lib.clo_append_kv.argtypes = [vp, i32, i32, vp, vp, i64, i32]
     lib.clo_decode_step.restype = ctypes.c_int
     lib.clo_decode_step.argtypes = [vp, vp, vp, i32]
+    lib.clo_append_step.restype = ctypes.c_int
+    lib.clo_append_step.argtypes = [vp, vp, vp, i32]
     lib.clo_decode_layer.restype = ctypes.c_int
     lib.clo_decode_layer.argtypes = [vp, i32, vp, vp, i32]
     lib.clo_sync.restype = ctypes.c_int
@@ -158,6 +161,13 @@ def clo_append_kv(ctx, layer: int, seq: int, k, v, n_tokens: int, src_is_device:
     vp_, vdev = _ptr(v)
     dev = kdev if src_is_device is None else bool(src_is_device)
     _check(load_library().clo_append_kv(ctx, layer, seq, kp, vp_, int(n_tokens), int(bool(dev))), "clo_append_kv")
+
+
+def clo_append_step(ctx, k, v, src_is_device: bool | None = None) -> None:
+    kp, kdev = _ptr(k)
+    vp_, vdev = _ptr(v)
+    dev = kdev if src_is_device is None else bool(src_is_device)
+    _check(load_library().clo_append_step(ctx, kp, vp_, int(bool(dev))), "clo_append_step")
 
 
 def clo_decode_step(ctx, q, out, io_on_device: bool | None = None) -> None:
@@ -264,6 +274,11 @@ class CLOContext:
         n = k.shape[0]
         clo_append_kv(self.ctx, layer, seq, k, v, n, src_is_device)
         self.ntok[layer, seq] += n
+
+    def append_step(self, k, v, src_is_device=None):
+        """One new token for every (layer, sequence): k, v bf16 [L][B][Hkv][d]."""
+        clo_append_step(self.ctx, k, v, src_is_device)
+        self.ntok += 1
 
     def decode_step(self, q, out, io_on_device=None):
         clo_decode_step(self.ctx, q, out, io_on_device)

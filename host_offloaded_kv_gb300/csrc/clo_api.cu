@@ -61,6 +61,8 @@ struct clo_ctx {
   bool warmup_mode = false;
   int kv_bits = 16;
   int whole_unit_min_units = 0;  // launches with at least this many units select units whole
+  uint16_t* kstep = nullptr;     // staging of clo_append_step's host rows
+  uint16_t* vstep = nullptr;
   int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
   int W = 0;
   bool warmup_done = false;
@@ -407,6 +409,40 @@ CLO_API clo_status clo_append_kv(clo_ctx* c, int32_t layer, int32_t seq, const v
   cur += n_tokens;
   c->ntok_dirty = true;
   return read_device_error(c);
+}
+
+static clo_status refresh_lengths(clo_ctx* c);
+
+CLO_API clo_status clo_append_step(clo_ctx* c, const void* k, const void* v, int32_t src_is_device) {
+  if (!c) return fail(CLO_ERR_INVALID, "null context");
+  if (!k || !v) return fail(CLO_ERR_INVALID, "null k/v");
+  if (c->next_layer != 0) return fail(CLO_ERR_STATE, "a layer-by-layer step is in progress");
+  for (int b = 0; b < c->B; ++b) {
+    const int64_t n0 = c->ntok[b];
+    for (int l = 1; l < c->L; ++l)
+      if (c->ntok[(size_t)l * c->B + b] != n0)
+        return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has layers of different lengths");
+    if (n0 < 1) return fail(CLO_ERR_STATE, "sequence " + std::to_string(b) + " has no K/V appended");
+    if (n0 + 1 > c->Nmax)
+      return fail(CLO_ERR_CAPACITY, "sequence " + std::to_string(b) + " is at max_tokens " + std::to_string(c->Nmax));
+  }
+  if (c->ntok_dirty) CLO_TRY(refresh_lengths(c));  // the device lengths are the current ones
+  const size_t n = (size_t)c->L * c->B * c->Hkv * c->d;
+  const uint16_t* kd = static_cast<const uint16_t*>(k);
+  const uint16_t* vd = static_cast<const uint16_t*>(v);
+  if (!src_is_device) {
+    if (!c->kstep) {
+      CLO_TRY(c->dalloc(&c->kstep, n));
+      CLO_TRY(c->dalloc(&c->vstep, n));
+    }
+    CLO_CUDA(cudaMemcpyAsync(c->kstep, k, sizeof(uint16_t) * n, cudaMemcpyHostToDevice, c->stream));
+    CLO_CUDA(cudaMemcpyAsync(c->vstep, v, sizeof(uint16_t) * n, cudaMemcpyHostToDevice, c->stream));
+    kd = c->kstep;
+    vd = c->vstep;
+  }
+  CLO_CUDA(launch_append_step(c->ds, kd, vd, c->cfg.topk, c->cfg.topk_ratio, c->stream));
+  for (auto& x : c->ntok) x += 1;  // the device lengths advance in the same stream
+  return CLO_OK;
 }
 
 static clo_status refresh_lengths(clo_ctx* c) {

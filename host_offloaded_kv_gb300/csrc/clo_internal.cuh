@@ -291,6 +291,8 @@ cudaError_t launch_step_fused(const DevState& s, const uint16_t* q, float* out, 
 cudaError_t launch_resident_fill(const DevState& s, int64_t t0, int64_t t1, cudaStream_t st);
 cudaError_t launch_pool_write(const DevState& s, int l, int b, int64_t t0, int64_t n, const uint16_t* kdev,
                               const uint16_t* vdev, cudaStream_t st);
+cudaError_t launch_append_step(const DevState& s, const uint16_t* kdev, const uint16_t* vdev, int64_t topk,
+                               double ratio, cudaStream_t st);
 
 
 }  // namespace clo

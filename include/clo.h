@@ -162,6 +162,21 @@ CLO_API clo_status clo_destroy(clo_ctx* ctx);
 CLO_API clo_status clo_append_kv(clo_ctx* ctx, int32_t layer, int32_t seq, const void* k, const void* v,
                                  int64_t n_tokens, int32_t src_is_device);
 
+/* Streaming growth ([SYN] 5.7: incremental offloading, the cache lookup and transfer
+ * engine updated as the KV cache grows): appends one token to every (layer,
+ * sequence) at its current length, asynchronously on the context's stream (no host
+ * synchronisation): the K|V records go to the host pool (and to the resident copy of
+ * persistent heads), the keys' hash codes are computed on the GPU, and each sequence's
+ * length N and top-k count k (the same rule as at offload) advance on the device, so
+ * the next clo_decode_step selects over N + 1 tokens.  A unit that reuses its
+ * selection keeps it as it was.
+ * k, v: bf16 [L][B][Hkv][d], device (src_is_device = 1) or host (0) memory; device
+ * buffers must stay valid until the stream has consumed them, host buffers are copied.
+ * Every layer of every sequence must hold the same number (>= 1) of tokens.
+ * Errors: CLO_ERR_INVALID, CLO_ERR_STATE (ragged layers, no K/V, layer-by-layer
+ * step in progress), CLO_ERR_CAPACITY (a sequence at max_tokens), CLO_ERR_CUDA. */
+CLO_API clo_status clo_append_step(clo_ctx* ctx, const void* k, const void* v, int32_t src_is_device);
+
 /* One decode step over all layers ([ABS]; [SYN] 2.1, 2.2):
  * q: bf16 [L][B][Hq][d]; out: fp32 [L][B][Hq][d].
  * io_on_device = 1: q and out are device pointers; the call only enqueues work on

@@ -244,6 +244,19 @@ class OracleCLO:
         self.kv[(l, b, h)] = (kv_roundtrip(K, self.kv_bits), kv_roundtrip(V, self.kv_bits))
         self.ntok[b] = K.shape[0]
 
+    def append_tokens(self, Knew, Vnew):
+        """Streaming growth ("CLO (2511.14510) - L3 Per-Paper Synthesis", section 5.7:
+        incremental offloading): one new token per (layer, sequence), bf16
+        [L][B][Hkv][d]; its key code joins the unit's codes and every length grows by 1."""
+        Knew = _c(Knew, np.uint16).reshape(self.L, self.B, self.Hkv, self.d)
+        Vnew = _c(Vnew, np.uint16).reshape(self.L, self.B, self.Hkv, self.d)
+        for (l, b, h), (K, V) in list(self.kv.items()):
+            kr, vr = Knew[l, b, h][None, :], Vnew[l, b, h][None, :]
+            self.kcodes[(l, b, h)] = np.concatenate([self.kcodes[(l, b, h)], hash_codes(kr, self.R[l, h])])
+            self.kv[(l, b, h)] = (np.concatenate([K, kv_roundtrip(kr, self.kv_bits)]),
+                                  np.concatenate([V, kv_roundtrip(vr, self.kv_bits)]))
+        self.ntok += 1
+
     def k_of(self, b: int) -> int:
         return topk_count(int(self.ntok[b]), self.topk_fixed, self.ratio)
 

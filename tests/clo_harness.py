@@ -95,6 +95,33 @@ class LockStep:
             want = self.orc.kcodes[u]
             assert np.array_equal(got, want), f"key codes differ for unit {u}"
 
+    def append_step(self, src_is_device=True):
+        """One new token for every (layer, sequence), from the seeded generator at each
+        sequence's current length; the library appends it on the device, the oracle on
+        its own copy."""
+        s = self.spec
+        Knew = np.empty((s.L, s.B, s.Hkv, s.d), dtype=np.uint16)
+        Vnew = np.empty_like(Knew)
+        for l in range(s.L):
+            for b in range(s.B):
+                K, V = self.syn.layer_seq_kv(l, b, s.Hkv, int(self.orc.ntok[b]), 1, s.d)
+                Knew[l, b], Vnew[l, b] = K[0], V[0]
+        if src_is_device:
+            kd = self.torch.from_numpy(Knew.view(np.int16)).cuda()
+            vd = self.torch.from_numpy(Vnew.view(np.int16)).cuda()
+            self.lib.append_step(kd, vd)
+            self.lib.sync()
+        else:
+            self.lib.append_step(Knew, Vnew, src_is_device=False)
+        self.orc.append_tokens(Knew, Vnew)
+        for l in range(s.L):
+            for b in range(s.B):
+                for h in range(s.Hkv):
+                    if (l, b, h) in self.kv:
+                        Kh, Vh = self.kv[(l, b, h)]
+                        self.kv[(l, b, h)] = (np.concatenate([Kh, Knew[l, b, h][None]]),
+                                              np.concatenate([Vh, Vnew[l, b, h][None]]))
+
     def step(self, q=None, check=True, io_on_device=True, per_layer=False):
         """One decode step through clo_decode_step, or (per_layer) through one
         clo_decode_layer call per layer; the oracle takes the whole step."""
