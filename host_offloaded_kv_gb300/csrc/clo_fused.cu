@@ -241,7 +241,17 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   const int w0 = warp * WSEG;
   const int w1 = (w0 + WSEG < len) ? w0 + WSEG : len;
   const uint4* src = s.codes + u * s.Nmax + t0;
+  constexpr int kPfRounds = 4;  // L2 prefetch of the codes this many rounds ahead
+  if (lane == 0)
+    for (int r = 1; r < kPfRounds; ++r) {
+      const int pb = w0 + r * 32 * kU;
+      if (pb < w1) prefetch_l2(src + pb, 16u * (uint32_t)((w1 - pb) < 32 * kU ? (w1 - pb) : 32 * kU));
+    }
   for (int base = w0; base < w1; base += 32 * kU) {
+    if (lane == 0) {
+      const int pb = base + kPfRounds * 32 * kU;
+      if (pb < w1) prefetch_l2(src + pb, 16u * (uint32_t)((w1 - pb) < 32 * kU ? (w1 - pb) : 32 * kU));
+    }
     uint4 cv[kU];
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
@@ -420,7 +430,17 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
   const int w0 = warp * WSEG;
   const int w1 = (w0 + WSEG < N) ? w0 + WSEG : N;
   const uint4* src = s.codes + u * s.Nmax;
+  constexpr int kPfRounds = 8;  // L2 prefetch of the codes this many rounds ahead
+  if (lane == 0)
+    for (int r = 1; r < kPfRounds; ++r) {
+      const int pb = w0 + r * 32 * kU;
+      if (pb < w1) prefetch_l2(src + pb, 16u * (uint32_t)((w1 - pb) < 32 * kU ? (w1 - pb) : 32 * kU));
+    }
   for (int base = w0; base < w1; base += 32 * kU) {
+    if (lane == 0) {
+      const int pb = base + kPfRounds * 32 * kU;
+      if (pb < w1) prefetch_l2(src + pb, 16u * (uint32_t)((w1 - pb) < 32 * kU ? (w1 - pb) : 32 * kU));
+    }
     uint4 cv[kU];
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
@@ -627,7 +647,22 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
     for (int c = 0; c < VPR / 2; ++c) cp_async16_zfill(dp + c * 8, sp + c, bytes);
     cp_async_commit();
   };
+  // L2 prefetch of the rows kPf chunks ahead (lane < 16: one row each), so the copies
+  // into shared memory find them in L2: more reads in flight than the two row buffers hold
+  constexpr int kPf = 4;
+  auto pf_row_of = [&](int64_t rb) -> int64_t {  // source row of lane's row in chunk rb, or -1
+    const int64_t t = rb + (lane & 15);
+    if (lane >= 16 || t >= r1) return -1;
+    if (!persistent) return t;
+    const int64_t v = __ldcg(ix + t);
+    return (v < 0 || v >= N) ? -1 : v;
+  };
   if (r0 < r1) {
+    for (int c = 2; c < kPf; ++c) {
+      const int64_t pr = pf_row_of(r0 + 16 * c);
+      if (pr >= 0) prefetch_l2(src + pr * VPR, 16u * VPR);
+    }
+    int64_t pf = pf_row_of(r0 + 16 * kPf);
     int64_t nxt = row_of(r0);
     if (NBUF == 2) {
       issue(r0, 0, nxt);
@@ -636,6 +671,8 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
     int ci = 0;
     for (int64_t rb = r0; rb < r1; rb += 16, ++ci) {
       const int buf = NBUF == 2 ? (ci & 1) : 0;
+      if (pf >= 0) prefetch_l2(src + pf * VPR, 16u * VPR);
+      pf = pf_row_of(rb + 16 * (kPf + 1));
       if (NBUF == 2) {
         if (rb + 16 < r1) {
           issue(rb + 16, buf ^ 1, nxt);
