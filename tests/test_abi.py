@@ -5,6 +5,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -62,6 +63,31 @@ def test_config_default_and_invalid_config_without_gpu(libpath):
         clo.clo_init(cfg)
     assert e.value.status == clo.CLO_ERR_INVALID
     assert "shapes" in clo.clo_last_error()
+
+
+_R = np.zeros((1, 1, 64, 128), dtype=np.uint16)
+
+
+def _valid_shapes(clo):
+    cfg = clo.clo_config_default()
+    cfg.n_layers, cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.max_tokens = 1, 1, 4, 1, 64, 128
+    cfg.hash_R = _R.ctypes.data
+    return cfg
+
+
+@pytest.mark.parametrize("field,value,text", [("kv_bits", 3, "kv_bits"), ("kv_bits", 8, "kv_bits"),
+                                              ("tau_ema", 0.0, "tau_ema"), ("tau_ema", 1.5, "tau_ema")])
+def test_invalid_extension_settings_without_gpu(libpath, field, value, text):
+    from host_offloaded_kv_gb300 import clo
+
+    cfg = _valid_shapes(clo)
+    assert cfg.kv_bits == 0 and abs(cfg.tau_ema - 0.0625) < 1e-15 and cfg.adaptive_tau == 0
+    cfg.adaptive_tau = 1
+    setattr(cfg, field, value)
+    with pytest.raises(clo.CLOError) as e:
+        clo.clo_init(cfg)
+    assert e.value.status == clo.CLO_ERR_INVALID
+    assert text in clo.clo_last_error()
 
 
 def test_struct_layout_matches_header(libpath):
