@@ -249,6 +249,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   // scores fit in its shared memory); longer ones in chunks of 16384 tokens by several
   s.sel_chunk = c->Nmax <= 32768 ? (int)c->Nmax : kSelChunkMax;
   s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
+  s.sel_chunk_miss = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
+  s.nch_miss = (int)((c->Nmax + s.sel_chunk_miss - 1) / s.sel_chunk_miss);
   {  // launches with few units split them into 8192-token chunks (see enqueue_layers)
     int sms = 0;
     CLO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -475,10 +477,17 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   // group when the launch has units enough to occupy the groups; otherwise (one layer
   // of a layer-by-layer step, small batches) in chunks of 8192 tokens by several
   // groups, which selects each unit sooner
+  // (missed units always use chunks: their fetch waits for the selection, and chunks
+  // select a unit sooner)
   const int64_t units = (int64_t)(l1 - l0) * c->B * c->Hkv;
-  if (c->Nmax <= 32768)
+  if (c->Nmax <= 32768) {
     s.sel_chunk = units >= c->whole_unit_min_units ? (int)c->Nmax : 8192;
+    s.sel_chunk_miss = 8192;
+  } else {
+    s.sel_chunk = s.sel_chunk_miss = kSelChunkMax;
+  }
   s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
+  s.nch_miss = (int)((c->Nmax + s.sel_chunk_miss - 1) / s.sel_chunk_miss);
   const bool warm = c->warmup_mode && c->step < c->W;
   s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
   const bool timed = c->cfg.timing != 0;

@@ -219,12 +219,10 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
 // item to the end, so the waits of steps 2 and 3 only target items already running
 // (provided at least nch groups run; the host checks this).
 template <int G>
-__device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int gtid) {
+__device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int CH, int NC, int gtid) {
   constexpr int NB = 128 * G + 1;
   constexpr int kU = 8;                          // code loads in flight per lane
-  const int CH = s.sel_chunk;                    // 8192 or 16384
-  const int WSEG = CH / kCompWarps;              // tokens per warp, a multiple of 32 * kU
-  const int NC = s.nch;
+  const int WSEG = CH / kCompWarps;              // tokens per warp (CH: 8192 or 16384), a multiple of 32 * kU
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
   const int k = s.kcount[b];
@@ -927,7 +925,7 @@ __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int 
     if (nr > 0) {
       if (lane == 0) {  // the unit's selection: compute groups, earlier in their queue
         const uint64_t tw = s.timeline ? global_timer_ns() : 0;
-        wait_flag(&s.sel_cnt[u], (uint32_t)s.nch, s);
+        wait_flag(&s.sel_cnt[u], (uint32_t)s.nch_miss, s);
         if (s.timeline) {
           const uint64_t t1 = global_timer_ns();
           atomicAdd(&s.timeline[TL_FETCH_WAIT_NS], t1 - tw);
@@ -987,8 +985,8 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     // compute queue: selection chunks of the missed units, then of the persistent units
     // (layer by layer, the chunks of a unit next to each other), then attention splits
     // of reused, persistent and missed units
-    const long long nh = a[0], np = a[1], nm = a[2], NC = s.nch, NS = s.nsplit;
-    const long long size[5] = {nm * NC, np * NC, nh * NS, np * NS, nm * NS};
+    const long long nh = a[0], np = a[1], nm = a[2], NC = s.nch, NCM = s.nch_miss, NS = s.nsplit;
+    const long long size[5] = {nm * NCM, np * NC, nh * NS, np * NS, nm * NS};
     sec_start[0] = 0;
     for (int i = 0; i < 5; ++i) sec_start[i + 1] = sec_start[i] + size[i];
   }
@@ -1028,13 +1026,16 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     const int32_t* lst = list == 2 ? s.miss_list : (list == 1 ? s.pers_list : s.hit_list);
     if (s.timeline && gtid == 0) s_t0 = global_timer_ns();
     if (sec <= 1) {  // selection chunk
-      const int p = (int)(j / NC), c = (int)(j % NC);
+      // missed units: chunks that select a unit soon (its fetch waits); persistent units:
+      // whole units when they fit one group (fewer, cheaper items), else chunks
+      const int nc = sec == 0 ? s.nch_miss : NC;
+      const int p = (int)(j / nc), c = (int)(j % nc);
       const int l = layer_of(pl, L, p);
       const int64_t u = lst[(int64_t)l * BH + (p - pl[l])];
-      if (NC == 1 && s.sel_chunk >= s.Nmax)
+      if (sec == 1 && NC == 1 && s.sel_chunk >= s.Nmax)
         sel_unit<G>(s, sm.unit, u, gtid);
       else
-        sel_chunk<G>(s, sm.sel, u, c, gtid);
+        sel_chunk<G>(s, sm.sel, u, c, sec == 0 ? s.sel_chunk_miss : s.sel_chunk, nc, gtid);
       if (s.timeline && gtid == 0) {
         const uint64_t t1 = global_timer_ns();
         atomicMax(&s.timeline[sec == 0 ? TL_SEL_MISS_END : TL_SEL_PERS_END], t1);
@@ -1100,7 +1101,8 @@ cudaError_t launch_v(const DevState& s, const uint16_t* q, float* out, cudaStrea
 template <int D, int G>
 cudaError_t launch_dg(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
   // the selection's waits need all chunks of a unit running at once
-  if (fused_grid<D, G, 1, 3, 2, kFetchUnroll>() < s.nch) return cudaErrorInvalidConfiguration;
+  const int nc = s.nch > s.nch_miss ? s.nch : s.nch_miss;
+  if (fused_grid<D, G, 1, 3, 2, kFetchUnroll>() < nc) return cudaErrorInvalidConfiguration;
   return launch_v<D, G, 1, 3, 2>(s, q, out, st);
 }
 

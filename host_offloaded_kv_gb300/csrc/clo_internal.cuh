@@ -86,8 +86,10 @@ struct DevState {
   uint32_t* fin_done;           // [U] threshold published (zeroed per step)
   uint32_t* cnt_done;           // [U] chunk counts published (zeroed per step)
   uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
-  int sel_chunk;                // tokens per selection chunk
-  int nch;                      // selection chunks per unit = ceil(Nmax / sel_chunk)
+  int sel_chunk;                // tokens per selection chunk of a persistent unit (Nmax: whole unit)
+  int nch;                      // selection chunks per persistent unit = ceil(Nmax / sel_chunk)
+  int sel_chunk_miss;           // tokens per selection chunk of a missed unit
+  int nch_miss;                 // selection chunks per missed unit
   int nbp;                      // histogram bins per chunk, padded (>= 128*G + 1)
   unsigned long long* timeline; // [kTimelineSlots] %globaltimer stamps of the step (timing mode), or null
   int64_t wait_timeout_ns;

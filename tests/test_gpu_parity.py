@@ -113,9 +113,12 @@ def test_hash_cancellations_take_the_exact_tiers():
 
 
 def test_whole_unit_selection_many_units():
-    # 2 layers x 38 sequences x 8 kv heads = 608 units: enough to select each unit whole
-    # with one compute group (the per-chunk path is covered by the smaller cases above);
-    # ragged lengths, G = 4
+    # 2 layers x 38 sequences x 8 kv heads = 608 units: enough for persistent units to be
+    # selected whole by one compute group each, while missed units use chunks (the smaller
+    # cases above cover chunks only); ragged lengths, G = 4, two persistent heads per layer
     ntok = [3000 - 37 * b for b in range(38)]
-    spec = Spec(L=2, B=38, Hq=32, Hkv=8, d=64, ntok=ntok, seed=61, tau=0.9, rho=(0.8, 0.99))
-    _run(spec, 3)
+    pm = np.zeros((2, 8), dtype=np.uint8)
+    pm[:, [0, 5]] = 1
+    spec = Spec(L=2, B=38, Hq=32, Hkv=8, d=64, ntok=ntok, seed=61, tau=0.9, rho=(0.8, 0.99), persist_mask=pm)
+    log = _run(spec, 3)
+    assert all(r["persist"] == 2 * 38 * 2 for r in log) and sum(r["miss"] for r in log) > 0
