@@ -59,7 +59,8 @@ def parse_args():
     p.add_argument("--layerwise", action="store_true",
                    help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-steps", type=int, default=2, help="oracle steps timed for the CPU baseline")
+    p.add_argument("--cpu-steps", type=int, default=24,
+                   help="oracle steps timed for the CPU baseline (about 10 s of CPU work on llama32k)")
     return p.parse_args()
 
 
