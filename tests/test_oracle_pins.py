@@ -469,3 +469,31 @@ def test_kv_quant_picks_the_nearest_level(bits):
             assert dist[q] <= dist.min() + 1e-6 * scale
             assert abs(y[g, i] - grid[q]) <= abs(grid[q]) * 2.0 ** -8 + 1e-30
         assert y[g][np.argmin(xf[g])] == mn
+
+
+def test_append_tokens_equals_prefill_of_the_longer_context():
+    # streaming growth: appending tokens one step at a time gives the same unit state (codes,
+    # rows, length, top-k count) as offloading the longer context at once
+    L, B, Hq, Hkv, d, N, extra = 1, 2, 4, 2, 64, 300, 5
+    syn = Synth(81)
+    R = syn.hash_matrices(L, Hkv, d)
+    grow = orc.OracleCLO(L, B, Hq, Hkv, d, R, tau=np.full(L * Hkv, 0.9), ntok=[N] * B, kv_bits=4)
+    full = orc.OracleCLO(L, B, Hq, Hkv, d, R, tau=np.full(L * Hkv, 0.9), ntok=[N + extra] * B, kv_bits=4)
+    rows = {}
+    for b in range(B):
+        K, V = syn.layer_seq_kv(0, b, Hkv, 0, N + extra, d)
+        rows[b] = (K, V)
+        for h in range(Hkv):
+            grow.set_unit_kv(0, b, h, np.ascontiguousarray(K[:N, h]), np.ascontiguousarray(V[:N, h]))
+            full.set_unit_kv(0, b, h, np.ascontiguousarray(K[:, h]), np.ascontiguousarray(V[:, h]))
+    for i in range(extra):
+        Knew = np.stack([rows[b][0][N + i] for b in range(B)])[None]
+        Vnew = np.stack([rows[b][1][N + i] for b in range(B)])[None]
+        grow.append_tokens(Knew, Vnew)
+    assert np.array_equal(grow.ntok, full.ntok)
+    for b in range(B):
+        assert grow.k_of(b) == full.k_of(b) == math.ceil(0.1 * (N + extra))
+        for h in range(Hkv):
+            assert np.array_equal(grow.kcodes[(0, b, h)], full.kcodes[(0, b, h)])
+            assert np.array_equal(grow.kv[(0, b, h)][0], full.kv[(0, b, h)][0])
+            assert np.array_equal(grow.kv[(0, b, h)][1], full.kv[(0, b, h)][1])
