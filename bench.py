@@ -407,8 +407,8 @@ def run_gb300(args, rank, world, local_rank):
         "config": {"workload": w.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
                    "head_dim": d, "context": N, "topk": kmax, "persistent_heads": w.n_persist if tau is None else 0,
                    "tau": (f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
-                           else w.tau_fixed) + (", then adaptive (running average, weight 1/16)"
-                                                if args.adaptive_tau else ""), "kv_dtype": "bf16" if args.kv_bits == 16 else
+                           else f"{w.tau_fixed} fixed") + (", then adaptive (running average, weight 1/16)"
+                                                           if args.adaptive_tau else ""), "kv_dtype": "bf16" if args.kv_bits == 16 else
                    f"int{args.kv_bits} host pool (asymmetric, 64-channel groups, fp32 scale/min), bf16 on the GPU", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
