@@ -466,16 +466,12 @@ def oracle_sample(args, steps, warm, layers_sampled=1):
             "seconds_timed": sec}
 
 
-def run_reference(args):
-    import torch
-
-    if torch.cuda.is_available() and not args.no_cpu_baseline:
-        pass
+def run_reference(args, world=1):
     K, W = args.steps, args.warmup
     # bounded: the oracle takes ~0.3-1 s per sampled layer-step; cap the timed steps
     cb = oracle_sample(args, steps=max(1, min(K, 8)), warm=min(W, 3))
     w = workload_from_args(args)
-    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 1,
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
             "steps": max(1, min(K, 8)), "warmup": min(W, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
             "config": {"workload": w.name}, "cpu_baseline": cb,
@@ -489,9 +485,9 @@ def main():
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
     if args.impl == "reference":
-        if rank != 0:
+        if rank != 0:   # the oracle runs once, on rank 0's host cores
             return 0
-        print(json.dumps(run_reference(args)))
+        print(json.dumps(run_reference(args, world)))
         return 0
     import torch
 
