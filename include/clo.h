@@ -210,7 +210,10 @@ CLO_API clo_status clo_decode_layer(clo_ctx* ctx, int32_t layer, const void* q, 
 CLO_API clo_status clo_sync(clo_ctx* ctx);
 
 /* Counters since clo_init (synchronises; also reports a latched device error
- * after filling *out). */
+ * after filling *out): the head-wise reuse decisions ([SYN] 2.1 item 2: reuse of
+ * the on-GPU selection when adjacent-step queries are similar), the bytes the
+ * fetch moved over the host link ([ABS] feature (3): the zero-copy transfer
+ * engine) and the algorithmic HBM bytes, per step and cumulative. */
 CLO_API clo_status clo_stats(clo_ctx* ctx, clo_stats_t* out);
 
 /* Thread-local text of the last failed call ("" if none). */
@@ -261,8 +264,10 @@ CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int3
 enum { CLO_SET_DROP_FLAG_LAYER = 1, CLO_SET_WAIT_TIMEOUT_NS = 2 };
 CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
 
-/* Split-K sparse decode attention that allocates nothing.  The paper has no
- * counterpart to this call; it is here for callers that are not allowed to
+/* Split-K sparse decode attention that allocates nothing: the attention over a
+ * top-k selection of the decode step ([SYN] 2.2: top-k = 10 % attention) on rows
+ * the caller provides.  The paper has no counterpart to this call as an entry
+ * point; it is here for callers that are not allowed to
  * allocate device memory themselves or through the library: a serving engine or
  * plugin host that plans every byte of device memory up front and hands kernels
  * only their inputs and outputs, or a latency-critical loop that cannot take the
