@@ -122,3 +122,29 @@ def test_whole_unit_selection_many_units():
     spec = Spec(L=2, B=38, Hq=32, Hkv=8, d=64, ntok=ntok, seed=61, tau=0.9, rho=(0.8, 0.99), persist_mask=pm)
     log = _run(spec, 3)
     assert all(r["persist"] == 2 * 38 * 2 for r in log) and sum(r["miss"] for r in log) > 0
+
+
+def test_cached_query_is_the_last_refresh():
+    # queries turning 20, 20, 15, 15, 10 degrees per step against tau = 0.9: the reuse test
+    # compares with the query of the unit's last refresh, so it misses at 40 and 70 degrees
+    # although every step is within tau of the previous one; head 1 is persistent
+    import math
+
+    from host_offloaded_kv_gb300.synth import float_to_bf16
+
+    d = 64
+    pm = np.array([[0, 1]], dtype=np.uint8)
+    spec = Spec(L=1, B=1, Hq=2, Hkv=2, d=d, ntok=[3000], seed=74, tau=0.9, persist_mask=pm)
+    ls = LockStep(spec)
+    try:
+        want = []
+        for theta in (0, 20, 40, 55, 70, 80):
+            q = np.zeros((1, 1, 2, d))
+            for h, a in ((0, theta), (1, theta + 90)):
+                q[0, 0, h, 0], q[0, 0, h, 1] = math.cos(math.radians(a)), math.sin(math.radians(a))
+            res, _, dec, _ = ls.step(q=float_to_bf16(q))
+            want.append(int(dec[0, 0, 0]))
+            assert dec[0, 0, 1] == 2
+        assert want == [1, 0, 1, 0, 1, 0]
+    finally:
+        ls.close()

@@ -497,3 +497,89 @@ def test_append_tokens_equals_prefill_of_the_longer_context():
             assert np.array_equal(grow.kcodes[(0, b, h)], full.kcodes[(0, b, h)])
             assert np.array_equal(grow.kv[(0, b, h)][0], full.kv[(0, b, h)][0])
             assert np.array_equal(grow.kv[(0, b, h)][1], full.kv[(0, b, h)][1])
+
+
+# --------------------------------------------------------------------------- cached query
+def _plane_query(theta_deg, d):
+    """bf16 query of unit norm at angle theta in the plane of the first two axes."""
+    x = np.zeros(d)
+    x[0], x[1] = math.cos(math.radians(theta_deg)), math.sin(math.radians(theta_deg))
+    return float_to_bf16(x)
+
+
+def test_state_cached_query_is_the_last_refresh_not_the_previous_step():
+    # Reuse test of "CLO (2511.14510) - L3 Per-Paper Synthesis" section 2.1 item 2 read
+    # as: compare with the query cached at the unit's last refresh (a miss), so slow
+    # drift still triggers a refresh.  Queries turn by 20, 20, 15, 15 degrees per step
+    # against tau = 0.9 (cos 20 = 0.940, cos 30 = 0.866, cos 40 = 0.766): every step is
+    # within tau of the previous one, so a cache refreshed on hits would hit at every step
+    # after the first.
+    d = 16
+    syn = Synth(71)
+    R = syn.hash_matrices(1, 1, d)
+    o = orc.OracleCLO(1, 1, 1, 1, d, R, topk_ratio=0.1, tau=np.array([0.9]))
+    K, V = syn.unit_kv(0, 0, 0, 0, 200, d)
+    o.set_unit_kv(0, 0, 0, K, V)
+    k = orc.topk_count(200, 0, 0.1)
+    plan = [(0, orc.DEC_MISS, None), (20, orc.DEC_HIT, 0), (40, orc.DEC_MISS, 0), (55, orc.DEC_HIT, 40),
+            (70, orc.DEC_MISS, 40), (80, orc.DEC_HIT, 70)]
+    for theta, want, ref in plan:
+        q = _plane_query(theta, d).reshape(1, 1, 1, d)
+        r = o.step(q)
+        assert r.decision[0, 0, 0] == want, (theta, r.cos[0, 0, 0])
+        if ref is None:
+            assert np.isnan(r.cos[0, 0, 0])
+        else:
+            # the cosine is taken against the query of the last refresh
+            assert abs(r.cos[0, 0, 0] - math.cos(math.radians(theta - ref))) < 0.01
+        assert r.host_bytes == (k * 4 * d if want == orc.DEC_MISS else 0)
+        if want == orc.DEC_MISS:
+            refresh_q, refresh_idx = q.copy(), r.idx[(0, 0, 0)].copy()
+            sc = orc.scores(orc.hash_codes(q.reshape(1, d), R[0, 0]), orc.hash_codes(K, R[0, 0]))
+            assert np.array_equal(refresh_idx, orc.topk(sc, k))
+        else:
+            assert np.array_equal(r.idx[(0, 0, 0)], refresh_idx)   # the refresh's selection
+        assert np.array_equal(o.qcache[0, 0, 0], refresh_q.reshape(-1))
+
+
+def test_state_persistent_unit_keeps_no_cached_query():
+    # persistent heads always reselect ([ABS] feature (2)); they never refresh the cached
+    # query, so head 1 stays without one while head 0 refreshes only on its misses
+    d, L, B, Hkv = 16, 1, 1, 2
+    syn = Synth(72)
+    R = syn.hash_matrices(L, Hkv, d)
+    mask = np.array([[False, True]])
+    o = orc.OracleCLO(L, B, 2, Hkv, d, R, topk_ratio=0.1, tau=np.full(2, 0.9), persist_mask=mask)
+    for h in range(Hkv):
+        o.set_unit_kv(0, 0, h, *syn.unit_kv(0, 0, h, 0, 100, d))
+    for theta in (0, 20, 40, 55):
+        q = np.stack([_plane_query(theta, d), _plane_query(theta + 90, d)]).reshape(1, 1, 2, d)
+        r = o.step(q)
+        assert r.decision[0, 0, 1] == orc.DEC_PERSIST
+        assert not o.qvalid[0, 0, 1] and not o.qcache[0, 0, 1].any()
+    assert r.decision[0, 0, 0] == orc.DEC_HIT
+    assert np.array_equal(o.qcache[0, 0, 0], _plane_query(40, d))
+
+
+def test_state_warmup_then_persistent_cache_frozen():
+    # after warm-up (all misses) the persistent head keeps the cached query of the last
+    # warm-up step: later steps neither compare against nor overwrite it
+    L, B, Hq, Hkv, d, W = 1, 1, 2, 2, 16, 3
+    syn = Synth(73)
+    R = syn.hash_matrices(L, Hkv, d)
+    o = orc.OracleCLO(L, B, Hq, Hkv, d, R, topk_ratio=0.1, tau=None, warmup_steps=W, tau_offset=0.05,
+                      n_persist=1)
+    for h in range(Hkv):
+        o.set_unit_kv(0, 0, h, *syn.unit_kv(0, 0, h, 0, 100, d))
+    # head 0 repeats (s_hat 1), head 1 turns 90 degrees each step (s_hat 0): head 1 persistent
+    for t in range(W):
+        q = np.stack([_plane_query(0, d), _plane_query(90 * t, d)]).reshape(1, 1, 2, d)
+        o.step(q)
+    assert o.persist.tolist() == [[False, True]]
+    frozen = o.qcache[0, 0, 1].copy()
+    assert np.array_equal(frozen, _plane_query(90 * (W - 1), d))
+    for t in range(3):
+        q = np.stack([_plane_query(0, d), _plane_query(45 * t + 10, d)]).reshape(1, 1, 2, d)
+        r = o.step(q)
+        assert r.decision[0, 0, 1] == orc.DEC_PERSIST and r.decision[0, 0, 0] == orc.DEC_HIT
+        assert np.array_equal(o.qcache[0, 0, 1], frozen)
