@@ -59,6 +59,9 @@ def parse_args():
     p.add_argument("--layerwise", action="store_true",
                    help="decode each step with one clo_decode_layer call per layer, in order")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--plan", action="store_true",
+                   help="print each rank's plan (device, seed, pool bytes, host-memory check) and exit: "
+                        "runs without a GPU")
     p.add_argument("--cpu-steps", type=int, default=24,
                    help="oracle steps timed for the CPU baseline (about 10 s of CPU work on llama32k)")
     return p.parse_args()
@@ -214,6 +217,22 @@ def whole_job_rate(units_per_rank: float, seconds_slowest: float, world: int) ->
     return world * units_per_rank / seconds_slowest
 
 
+def kernel_roofline(hbm_bytes: float, host_bytes: float, ms: float, hbm_peak_gbs: float, link_peak_gbs: float):
+    """Roofline of one launch from its algorithmic bytes: the bound is whichever side
+    needs more time at its peak (HBM bytes at the HBM peak, host bytes at the link
+    peak); both fractions are reported."""
+    sec = ms / 1e3
+    hbm_gbs = hbm_bytes / sec / 1e9
+    link_gbs = host_bytes / sec / 1e9
+    t_hbm = hbm_bytes / (hbm_peak_gbs * 1e9)
+    t_link = host_bytes / (link_peak_gbs * 1e9)
+    bound = "hbm" if t_hbm >= t_link else "host-link"
+    achieved, peak = (hbm_gbs, hbm_peak_gbs) if bound == "hbm" else (link_gbs, link_peak_gbs)
+    return {"bound": bound, "achieved": achieved, "peak": peak, "frac": achieved / peak,
+            "hbm_gbs": hbm_gbs, "link_gbs": link_gbs, "frac_hbm": hbm_gbs / hbm_peak_gbs,
+            "frac_link": link_gbs / link_peak_gbs}
+
+
 # ----------------------------------------------------------------------------- workload
 def workload_from_args(args):
     from host_offloaded_kv_gb300.synth import get_workload
@@ -224,6 +243,50 @@ def workload_from_args(args):
     if args.batch:
         w = w.scaled(batch=args.batch)
     return w
+
+
+def rank_plan(args, rank, world, local_rank):
+    """What one replica runs: its device, its own seed (independent sequences per rank)
+    and the bytes of its pinned host pool."""
+    w = workload_from_args(args)
+    rec_bytes = 4 * w.head_dim if args.kv_bits == 16 else 2 * w.head_dim * args.kv_bits // 8 + (2 * w.head_dim // 64) * 8
+    n_grow = ((w.warmup_steps if w.tau_fixed is None else 0) + args.warmup + 2 * args.steps + 1) if args.grow else 0
+    ncap = w.n_tokens + n_grow
+    pool = w.n_layers * w.batch * w.n_kv_heads * ncap * rec_bytes
+    return {"rank": rank, "world": world, "local_rank": local_rank, "device": f"cuda:{local_rank}",
+            "seed": w.seed + 1000 * rank, "workload": w.name, "batch": w.batch, "max_tokens": ncap,
+            "pool_bytes": pool, "host_need_bytes": int(pool * 1.15) + (1 << 30)}
+
+
+def host_memory_check(plan, world, avail=None):
+    """All replicas of one node pin their pools in the same host memory: the sum of their
+    needs must fit what was available before any of them allocated.  Returns (ok, total
+    need, available)."""
+    avail = mem_available_bytes() if avail is None else avail
+    need = plan["host_need_bytes"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+        t = torch.tensor([float(need)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        need = int(t.item())
+        avail = int(max_over_ranks(-avail, world) * -1)   # the smallest reading
+    return need <= avail, need, avail
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Starts n replicas of this script on this node under torch.distributed.run (one
+    process per GPU, rendezvous on 127.0.0.1) and returns their launcher's exit code."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 def topk_of(w):
@@ -245,8 +308,10 @@ def run_gb300(args, rank, world, local_rank):
     n_grow = (w.warmup_steps if w.tau_fixed is None else 0) + W + 2 * K + 1 if args.grow else 0
     Ncap = N + n_grow                       # growth appends one token per step
     pool_bytes = L * B * Hkv * Ncap * rec_bytes
-    if mem_available_bytes() < pool_bytes * 1.15 + (1 << 30):
-        raise SystemExit(f"not enough host memory for the {pool_bytes / 2**30:.1f} GiB pinned pool of {w.name}")
+    ok, need, avail = host_memory_check(rank_plan(args, rank, world, local_rank), world)
+    if not ok:
+        raise SystemExit(f"not enough host memory for {world} pinned pool(s) of {w.name}: need "
+                         f"{need / 2**30:.1f} GiB, {avail / 2**30:.1f} GiB available")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.Stream(device=dev)
@@ -354,18 +419,24 @@ def run_gb300(args, rank, world, local_rank):
             qpin[i].copy_(torch.from_numpy(qh.view(np.int16)))
         opin = torch.empty((L, B, Hq, d), dtype=torch.float32, pin_memory=True)
         step_fn(qpin[0].numpy(), opin.numpy(), io_on_device=False)
-        lib.stats()
+        e_before = lib.stats()
         if world > 1:
             torch.distributed.barrier()
         t1 = time.perf_counter()
         for i in range(1, Ke):
             step_fn(qpin[i].numpy(), opin.numpy(), io_on_device=False)
         t2 = time.perf_counter()
-        lib.stats()
+        e_after = lib.stats()
         sec = max_over_ranks(t2 - t1, world)
+        e_hit = e_after["units_hit"] - e_before["units_hit"]
+        e_miss = e_after["units_miss"] - e_before["units_miss"]
+        # the e2e steps continue the query stream after the device-timed ones, so their
+        # reuse decisions (and host bytes) differ: both regions report theirs
         e2e = {"value": whole_job_rate(B * (Ke - 1), sec, world), "unit": UNIT,
                "h2d_bytes_per_step": L * B * Hq * d * 2 + (2 * L * B * Hkv * d * 2 if args.grow else 0),
-               "d2h_bytes_per_step": L * B * Hq * d * 4}
+               "d2h_bytes_per_step": L * B * Hq * d * 4, "steps": Ke - 1,
+               "host_link_bytes_per_step": (e_after["host_bytes"] - e_before["host_bytes"]) / (Ke - 1),
+               "hit_rate_nonpersistent": e_hit / max(1, e_hit + e_miss)}
 
     link_gbs = max(link_gbs_before, pinned_h2d_gbs(dev))
     lib.close()
@@ -375,29 +446,22 @@ def run_gb300(args, rank, world, local_rank):
     steps = K
     tokens = world * B * steps
     value = whole_job_rate(B * steps, ms_total / 1e3, world)
-    # algorithmic bytes per phase (per timed region)
-    rec = 4 * d
-    fetch_bytes = host_bytes                       # host -> slot rows (read over the link)
-    attend_hbm = (hits + miss + pers) * kmax * rec + pers * kmax * 4
-    select_hbm = (miss + pers) * (N * 16 + kmax * 4)
-    kern = {}
-    for p in phases:
-        kern[p] = {"ms_per_launch": phases[p] / steps}
-    fu_s = phases["fused"] / 1e3
-    kern["fused"].update(
-        bound="host-link", achieved_gbs=fetch_bytes / fu_s / 1e9 if fetch_bytes else 0.0, peak_gbs=link_gbs,
-        hbm_gbs=(attend_hbm + fetch_bytes + select_hbm) / fu_s / 1e9,
-        note="host bytes over the link / kernel time; hbm_gbs = (code reads and index writes of the selections "
-             "+ attention row reads + slot writes) / kernel time")
-    dom = "fused"
-    dk = kern[dom]
+    kern = {p: {"ms_per_launch": phases[p] / steps} for p in phases}
+    # the fused kernel's algorithmic bytes per launch: HBM from the library's counter
+    # (codes read once per selected unit, index writes and reads, attention rows, bf16
+    # slot writes of the fetched rows, queries and outputs; the decide kernel's query and
+    # cached-query bytes, under 0.1 %, are included) and the host bytes over the link
+    fused_ms = phases["fused"] / steps
+    roof = kernel_roofline(hbm_bytes / steps, host_bytes / steps, fused_ms, hbm_peak, link_gbs)
+    kern["fused"].update(hbm_gbs=roof["hbm_gbs"], link_gbs=roof["link_gbs"], frac_hbm=roof["frac_hbm"],
+                         frac_link=roof["frac_link"], bound=roof["bound"])
     traffic = traffic_from_profiles("k_step_fused", w.name)
-    roofline = {"kernel": "k_step_fused",
-                "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"], "unit": "GB/s",
-                "frac": (dk["achieved_gbs"] / dk["peak_gbs"]) if dk["achieved_gbs"] else None,
-                "traffic": traffic,
-                "peak_source": ("pinned H2D copy, best of 16 timed 1 GiB copies in this run" if dk["bound"] == "host-link"
-                                else f"MEASURED_PEAKS.json hbm_gbs ({hbm_src})")}
+    roofline = {"kernel": "k_step_fused", "bound": roof["bound"], "achieved": roof["achieved"],
+                "peak": roof["peak"], "unit": "GB/s", "frac": roof["frac"], "traffic": traffic,
+                "frac_hbm": roof["frac_hbm"], "frac_link": roof["frac_link"],
+                "hbm_bytes_per_launch": hbm_bytes / steps, "host_bytes_per_launch": host_bytes / steps,
+                "peak_source": {"hbm": f"MEASURED_PEAKS.json hbm_gbs ({hbm_src})",
+                                "host-link": "pinned H2D copy, best of 16 timed 1 GiB copies in this run"}}
     step_ideal_ms = max(hbm_bytes / (hbm_peak * 1e9), host_bytes / (link_gbs * 1e9)) * 1e3 / steps
     step_ms = ms_total / steps
     return {
@@ -412,7 +476,8 @@ def run_gb300(args, rank, world, local_rank):
                    f"int{args.kv_bits} host pool (asymmetric, 64-channel groups, fp32 scale/min), bf16 on the GPU", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
-                   "hit_rate_nonpersistent": hits / max(1, hits + miss), "setup_s": round(t_setup, 1),
+                   "hit_rate_nonpersistent": hits / max(1, hits + miss),
+                   "host_link_bytes_per_step": host_bytes / steps, "setup_s": round(t_setup, 1),
                    "mode": ("layer by layer (clo_decode_layer per layer)" if args.layerwise else "whole step")
                    + (f", growing context: one token appended per step (clo_append_step), {N} -> {Ncap - 1} tokens"
                       if args.grow else "")},
@@ -479,11 +544,39 @@ def run_reference(args, world=1):
     return line
 
 
+def print_plan(args, rank, world, local_rank) -> int:
+    """--plan: every replica derives its plan; rank 0 prints all of them (gloo when the
+    node has no GPU) with the node's aggregate host-memory check."""
+    import torch
+
+    plan = rank_plan(args, rank, world, local_rank)
+    plans = [plan]
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        plans = [None] * world
+        dist.all_gather_object(plans, plan)
+    ok, need, avail = host_memory_check(plan, world)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps({"plan": plans, "host_need_bytes": need, "host_available_bytes": avail, "fits": ok}))
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # launched directly: start one replica per GPU (the same command under torchrun)
+        return spawn_ranks(args.gpus, sys.argv[1:])
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
+    if world != args.gpus and "WORLD_SIZE" in os.environ:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.plan:
+        return print_plan(args, rank, world, local_rank)
     if args.impl == "reference":
         if rank != 0:   # the oracle runs once, on rank 0's host cores
             return 0

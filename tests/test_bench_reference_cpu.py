@@ -21,3 +21,17 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_kernel_roofline_takes_the_side_that_needs_more_time():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # host bytes dominate: 0.95 GB at 211 GB/s (4.5 ms) vs 5.26 GB at 6812.7 GB/s (0.77 ms)
+    r = bench.kernel_roofline(5.26e9, 0.95e9, 4.766, 6812.7, 211.1)
+    assert r["bound"] == "host-link" and r["peak"] == 211.1
+    assert abs(r["frac"] - 0.95e9 / 4.766e-3 / 211.1e9) < 1e-12
+    assert abs(r["frac_hbm"] - 5.26e9 / 4.766e-3 / 6812.7e9) < 1e-12
+    # a pool of 2-bit codes and no persistent copies: HBM bytes dominate
+    r = bench.kernel_roofline(6.0e9, 0.02e9, 2.0, 6812.7, 211.1)
+    assert r["bound"] == "hbm" and r["achieved"] == r["hbm_gbs"] and r["frac"] == r["frac_hbm"]
