@@ -347,6 +347,7 @@ def run_gb300(args, rank, world, local_rank):
             syn.layer_seq_kv(l, b, Hkv, 0, N, d, Kbuf, Vbuf)
             lib.append_kv(l, b, Kbuf, Vbuf, src_is_device=False)
     t_setup = time.time() - t0
+    pool_node = lib.pool_node()
     del Kbuf, Vbuf
 
     if args.grow:   # the appended tokens' rows, from the generator at positions N, N+1, ...
@@ -478,6 +479,7 @@ def run_gb300(args, rank, world, local_rank):
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss),
                    "host_link_bytes_per_step": host_bytes / steps, "setup_s": round(t_setup, 1),
+                   "pool_numa_node": pool_node,
                    "mode": ("layer by layer (clo_decode_layer per layer)" if args.layerwise else "whole step")
                    + (f", growing context: one token appended per step (clo_append_step), {N} -> {Ncap - 1} tokens"
                       if args.grow else "")},

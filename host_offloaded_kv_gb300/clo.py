@@ -18,7 +18,7 @@ CLO_OK, CLO_ERR_INVALID, CLO_ERR_OOM, CLO_ERR_CUDA, CLO_ERR_TIMEOUT, CLO_ERR_STA
     CLO_ERR_DEVICE = range(8)
 CLO_DEC_HIT, CLO_DEC_MISS, CLO_DEC_PERSIST = 0, 1, 2
 (CLO_DBG_KEY_CODES, CLO_DBG_QUERY_CODES, CLO_DBG_IDX, CLO_DBG_DECISION, CLO_DBG_SLOT_ROWS, CLO_DBG_TAU,
- CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS, CLO_DBG_TIMELINE) = range(1, 11)
+ CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS, CLO_DBG_TIMELINE, CLO_DBG_TOPK, CLO_DBG_POOL_NODE) = range(1, 13)
 CLO_SET_DROP_FLAG_LAYER, CLO_SET_WAIT_TIMEOUT_NS = 1, 2
 
 _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ERR_CUDA", 4: "CLO_ERR_TIMEOUT",
@@ -206,7 +206,29 @@ def clo_set(ctx, key: int, value: int) -> None:
 
 def clo_sparse_attention_noalloc(q, rows, out, n_groups: int, group_size: int, head_dim: int, k: int,
                                  stream=None) -> None:
-    """Allocation-free sparse attention (device buffers; see include/clo.h)."""
+    """Allocation-free sparse attention (device buffers; see include/clo.h).
+
+    q: bf16 (int16/uint16 bit patterns) [n_groups][group_size][head_dim], rows: bf16
+    [n_groups][>= k][2][head_dim], out: fp32 [n_groups][group_size][head_dim]; all
+    three CUDA tensors on the current device.  Plain integers are passed through as raw
+    device addresses (the caller vouches for them)."""
+    import torch
+
+    G, D, n = int(group_size), int(head_dim), int(n_groups)
+    want = {"q": (q, n * G * D, (torch.int16, torch.uint16, torch.bfloat16)),
+            "rows": (rows, n * int(k) * 2 * D, (torch.int16, torch.uint16, torch.bfloat16)),
+            "out": (out, n * G * D, (torch.float32,))}
+    for name, (t, numel, dtypes) in want.items():
+        if isinstance(t, int):
+            continue
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.device.index != torch.cuda.current_device():
+            raise ValueError(f"{name} is on {t.device}, not on the current device")
+        if t.dtype not in dtypes:
+            raise ValueError(f"{name} has dtype {t.dtype}; expected one of {dtypes}")
+        if (t.numel() < numel) if name == "rows" else (t.numel() != numel):
+            raise ValueError(f"{name} holds {t.numel()} elements; expected {numel}")
     qp, _ = _ptr(q)
     rp, _ = _ptr(rows)
     op, _ = _ptr(out)
@@ -263,12 +285,14 @@ class CLOContext:
         except Exception:
             pass
 
-    def k_of(self, b: int) -> int:
-        import math
-        N = int(self.ntok[0, b])
-        if self.topk > 0:
-            return min(self.topk, N)
-        return max(1, min(N, int(math.ceil(self.topk_ratio * N))))
+    def pool_node(self) -> int:
+        """NUMA node of the pinned pool's pages, or -1 when the pool was not placed."""
+        return int(clo_debug_get(self.ctx, CLO_DBG_POOL_NODE, 0, 0, 0, np.empty(1, dtype=np.int32))[0])
+
+    def k_of(self, b: int, layer: int = 0) -> int:
+        """The library's top-k count of (layer, sequence b) at its current length."""
+        k = clo_debug_get(self.ctx, CLO_DBG_TOPK, 0, 0, 0, np.empty((self.L, self.B), dtype=np.int32))
+        return int(k[layer, b])
 
     def append_kv(self, layer, seq, k, v, src_is_device=None):
         n = k.shape[0]
@@ -305,11 +329,11 @@ class CLOContext:
         return clo_debug_get(self.ctx, CLO_DBG_QUERY_CODES, l, b, h, np.empty((self.G, 2), dtype=np.uint64))
 
     def idx(self, l, b, h):
-        return clo_debug_get(self.ctx, CLO_DBG_IDX, l, b, h, np.empty(self.k_of(b), dtype=np.int32))
+        return clo_debug_get(self.ctx, CLO_DBG_IDX, l, b, h, np.empty(self.k_of(b, l), dtype=np.int32))
 
     def slot_rows(self, l, b, h):
         return clo_debug_get(self.ctx, CLO_DBG_SLOT_ROWS, l, b, h,
-                             np.empty((self.k_of(b), 2, self.d), dtype=np.uint16))
+                             np.empty((self.k_of(b, l), 2, self.d), dtype=np.uint16))
 
     def decisions(self):
         return clo_debug_get(self.ctx, CLO_DBG_DECISION, 0, 0, 0,

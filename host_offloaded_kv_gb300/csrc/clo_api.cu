@@ -6,6 +6,9 @@
 // context's stream; no host synchronisation happens between layers or phases
 // (GPU-centric synchronisation: CLO abstract, feature (3)).
 #include <cuda_runtime.h>
+#include <sys/mman.h>
+#include <sys/syscall.h>
+#include <unistd.h>
 
 #include <algorithm>
 #include <array>
@@ -44,6 +47,80 @@ int64_t topk_for(int64_t N, int64_t topk, double ratio) {
   return std::max<int64_t>(1, std::min<int64_t>(k, N));
 }
 
+
+// ---- placement of the pinned pool ----------------------------------------------------
+// On a host with several NUMA nodes the pool's pages belong on the node nearest the
+// GPU (the node of its PCI function), so that the fetch's loads do not cross the
+// inter-socket link.  The pool is then an anonymous mapping whose pages are preferred
+// on that node, registered with CUDA as mapped, portable pinned memory; on a host with
+// one memory node (or if any step fails) it is plain cudaHostAlloc memory.
+
+// NUMA node of the device's PCI function, or -1 when unknown.
+int device_numa_node(int dev) {
+  char bus[64] = {0};
+  if (cudaDeviceGetPCIBusId(bus, (int)sizeof(bus), dev) != cudaSuccess) return -1;
+  unsigned dom = 0, b = 0, d = 0, f = 0;
+  if (sscanf(bus, "%x:%x:%x.%x", &dom, &b, &d, &f) != 4) return -1;
+  char path[128];
+  snprintf(path, sizeof(path), "/sys/bus/pci/devices/%04x:%02x:%02x.%x/numa_node", dom, b, d, f);
+  FILE* fp = fopen(path, "r");
+  if (!fp) return -1;
+  int node = -1;
+  if (fscanf(fp, "%d", &node) != 1) node = -1;
+  fclose(fp);
+  return node;
+}
+
+// Number of NUMA nodes that hold memory (sysfs "has_memory" list, e.g. "0-1" or "0,2").
+int memory_node_count() {
+  FILE* fp = fopen("/sys/devices/system/node/has_memory", "r");
+  if (!fp) return 1;
+  char buf[256] = {0};
+  const size_t n = fread(buf, 1, sizeof(buf) - 1, fp);
+  fclose(fp);
+  buf[n] = 0;
+  int count = 0;
+  for (char* t = buf; *t;) {
+    char* end = nullptr;
+    const long a = strtol(t, &end, 10);
+    if (end == t) break;
+    long bnd = a;
+    if (*end == '-') {
+      char* e2 = nullptr;
+      bnd = strtol(end + 1, &e2, 10);
+      end = e2;
+    }
+    count += (int)(bnd - a + 1);
+    t = end;
+    while (*t == ',' || *t == '\n' || *t == ' ') ++t;
+  }
+  return count > 0 ? count : 1;
+}
+
+// Pinned, device-mapped pool of `bytes` bytes with pages preferred on `node`; nullptr if
+// any step fails (nothing is left allocated then).
+void* alloc_pool_on_node(size_t bytes, int node) {
+  void* p = mmap(nullptr, bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (p == MAP_FAILED) return nullptr;
+  unsigned long mask[16] = {0};
+  if (node < 0 || node >= (int)(sizeof(mask) * 8)) {
+    munmap(p, bytes);
+    return nullptr;
+  }
+  mask[node / 64] = 1ul << (node % 64);
+  constexpr int kMpolPreferred = 1;  // MPOL_PREFERRED: that node first, others when it is full
+  if (syscall(SYS_mbind, p, bytes, kMpolPreferred, mask, (unsigned long)(sizeof(mask) * 8), 0u) != 0) {
+    munmap(p, bytes);
+    return nullptr;
+  }
+  madvise(p, bytes, MADV_HUGEPAGE);  // a hint; large pages are not required
+  if (cudaHostRegister(p, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+    cudaGetLastError();
+    munmap(p, bytes);
+    return nullptr;
+  }
+  return p;
+}
 }  // namespace
 
 struct clo_ctx {
@@ -52,6 +129,9 @@ struct clo_ctx {
   int64_t Nmax = 0, kmax = 0, U = 0;
   cudaStream_t stream = nullptr;
   uint16_t* pool_host = nullptr;
+  size_t pool_bytes = 0;
+  bool pool_registered = false;  // anonymous mapping registered with CUDA (else cudaHostAlloc)
+  int pool_node = -1;            // NUMA node the pool's pages prefer (-1: not placed)
   DevState ds{};
   std::vector<void*> dev_allocs;
   std::vector<int64_t> ntok;  // [L*B] tokens appended per (layer, seq)
@@ -61,6 +141,7 @@ struct clo_ctx {
   bool warmup_mode = false;
   int kv_bits = 16;
   int whole_unit_min_units = 0;  // launches with at least this many units select units whole
+  int sms = 0;                   // multiprocessors of the device
   uint16_t* kstep = nullptr;     // staging of clo_append_step's host rows
   uint16_t* vstep = nullptr;
   int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
@@ -97,7 +178,14 @@ struct clo_ctx {
     if (stream) cudaStreamSynchronize(stream);
     for (void* p : dev_allocs) cudaFree(p);
     dev_allocs.clear();
-    if (pool_host) cudaFreeHost(pool_host);
+    if (pool_host) {
+      if (pool_registered) {
+        cudaHostUnregister(pool_host);
+        munmap(pool_host, pool_bytes);
+      } else {
+        cudaFreeHost(pool_host);
+      }
+    }
     pool_host = nullptr;
     if (ntok_pinned) cudaFreeHost(ntok_pinned);
     ntok_pinned = nullptr;
@@ -188,9 +276,20 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
                                       : (size_t)2 * c->d * c->kv_bits / 8 + (size_t)(2 * c->d / 64) * 8;
   const size_t pool_bytes = (size_t)c->U * (size_t)c->Nmax * rec;
   void* hp = nullptr;
-  cudaError_t e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
-  if (e != cudaSuccess)
-    return fail(CLO_ERR_OOM, "cudaHostAlloc(" + std::to_string(pool_bytes) + " B pinned pool): " + cudaGetErrorString(e));
+  c->pool_bytes = pool_bytes;
+  if (memory_node_count() > 1) {  // several memory nodes: the pool's pages near the GPU
+    const int node = device_numa_node(dev);
+    if (node >= 0 && (hp = alloc_pool_on_node(pool_bytes, node)) != nullptr) {
+      c->pool_registered = true;
+      c->pool_node = node;
+    }
+  }
+  if (!hp) {
+    cudaError_t e = cudaHostAlloc(&hp, pool_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess)
+      return fail(CLO_ERR_OOM, "cudaHostAlloc(" + std::to_string(pool_bytes) + " B pinned pool): " +
+                                   cudaGetErrorString(e));
+  }
   c->pool_host = static_cast<uint16_t*>(hp);
   void* pd = nullptr;
   CLO_CUDA(cudaHostGetDevicePointer(&pd, hp, 0));
@@ -213,6 +312,7 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   s.drop_flag_layer = cfg->debug_drop_flag_layer;
   s.nsplit = (int)((c->kmax + kSplitRows - 1) / kSplitRows);
   s.nchunk = (int)((c->kmax + kChunkRows - 1) / kChunkRows);
+  s.fetch_rows = kChunkRows;
   const int64_t U = c->U;
   const int LH = c->L * c->Hkv;
   int64_t* ntok_d = nullptr;
@@ -255,8 +355,9 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     int sms = 0;
     CLO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     c->whole_unit_min_units = 4 * sms;
+    c->sms = sms;
   }
-  const int nch_max = (int)((c->Nmax + 8191) / 8192);
+  const int nch_max = (int)((c->Nmax + kSelChunkMin - 1) / kSelChunkMin);
   s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
   {
     size_t off = 2 * (size_t)C_NUM * kCtrLanes;
@@ -308,7 +409,7 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
   CLO_TRY(c->dalloc(&s.err, 1));
   CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));
-  CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * kPartsPerSplit * c->G * (c->d + 2)));
+  CLO_TRY(c->dalloc(&s.part, (size_t)U * s.nsplit * c->G * (c->d + 2)));
 
   std::vector<int32_t> pslot((size_t)LH, -1);
   std::vector<uint8_t> pm((size_t)LH, 0);
@@ -480,14 +581,22 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   // (missed units always use chunks: their fetch waits for the selection, and chunks
   // select a unit sooner)
   const int64_t units = (int64_t)(l1 - l0) * c->B * c->Hkv;
-  if (c->Nmax <= 32768) {
-    s.sel_chunk = units >= c->whole_unit_min_units ? (int)c->Nmax : 8192;
-    s.sel_chunk_miss = 8192;
-  } else {
-    s.sel_chunk = s.sel_chunk_miss = kSelChunkMax;
-  }
-  s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
-  s.nch_miss = (int)((c->Nmax + s.sel_chunk_miss - 1) / s.sel_chunk_miss);
+  // chunks of 8192 (contexts up to 32K) or 16384 tokens, halved (down to 1024) while the
+  // launch's units would give fewer than 4 chunks per SM: a launch with few units (one
+  // layer, a small batch) spreads each selection over more compute groups.  All chunks
+  // of a unit run at once (their waits need it), so a unit has at most one chunk per SM.
+  int chunk = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
+  auto nchunks = [&](int ch) { return (c->Nmax + ch - 1) / ch; };
+  while (chunk > kSelChunkMin && units * nchunks(chunk) < 4LL * c->sms && nchunks(chunk / 2) <= c->sms) chunk /= 2;
+  s.sel_chunk_miss = chunk;
+  s.sel_chunk = (c->Nmax <= 32768 && units >= c->whole_unit_min_units) ? (int)c->Nmax : chunk;
+  s.nch = (int)nchunks(s.sel_chunk);
+  s.nch_miss = (int)nchunks(s.sel_chunk_miss);
+  // fetch items: 256 rows, or smaller while the launch's selected rows would give fewer
+  // than 2 items per SM's fetch warps (3 per SM)
+  int frows = kChunkRows;
+  while (frows > 32 && units * c->kmax / frows < 6LL * c->sms) frows /= 2;
+  s.fetch_rows = frows;
   const bool warm = c->warmup_mode && c->step < c->W;
   s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
   const bool timed = c->cfg.timing != 0;
@@ -679,6 +788,18 @@ CLO_API clo_status clo_debug_get(clo_ctx* c, int32_t what, int32_t layer, int32_
       src = c->timeline_dev;
       bytes = (int64_t)kTimelineSlots * 8;
       break;
+    case CLO_DBG_POOL_NODE: {  // host-side value
+      if (dst_bytes < 4) return fail(CLO_ERR_INVALID, "dst too small: need 4 bytes");
+      *static_cast<int32_t*>(dst) = c->pool_node;
+      return read_device_error(c);
+    }
+    case CLO_DBG_TOPK: {  // host-side values: the same rule as the device's counts
+      if (dst_bytes < (int64_t)c->L * c->B * 4)
+        return fail(CLO_ERR_INVALID, "dst too small: need " + std::to_string((int64_t)c->L * c->B * 4) + " bytes");
+      int32_t* kd = static_cast<int32_t*>(dst);
+      for (size_t i = 0; i < c->ntok.size(); ++i) kd[i] = (int32_t)topk_for(c->ntok[i], c->cfg.topk, c->cfg.topk_ratio);
+      return read_device_error(c);
+    }
     default:
       return fail(CLO_ERR_INVALID, "unknown debug item " + std::to_string(what));
   }

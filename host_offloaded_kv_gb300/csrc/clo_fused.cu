@@ -1,34 +1,34 @@
-// One persistent, warp-specialised kernel per decode step: selection of the
-// persistent units, zero-copy fetch of missed heads' rows and split-K sparse
-// attention, ordered by device-side flags only.  (Missed units are selected by the
-// launch just before, so their fetch can start as soon as this kernel does.)
+// One persistent, warp-specialised kernel per decode step (or per layer): top-k
+// selection of the missed and persistent units, zero-copy fetch of the missed units'
+// rows from pinned host memory, and split-K sparse attention, ordered by device-side
+// flags only.  The reuse decisions, query codes and per-layer work lists come from the
+// decide kernel launched just before.
 //
-// Each CTA holds one fetch warp and one 4-warp compute group (3 CTAs per SM).  One
-// fetch warp per CTA keeps enough host-link requests in flight to saturate the link
-// without queueing so many that the HBM traffic of the compute groups waits behind
-// them.
-//   * The compute group takes items from one queue, in this order:
-//       1. selection of the persistent units, layer by layer:
-//          score chunk  -> histogram of the chunk's scores (codes streamed into shared
-//                          memory by 1-D bulk copies on the TMA engine);
-//          finalize     -> threshold score T of the unit and each chunk's output offset
-//                          and tie quota (ties go to the lowest token index);
-//          compact chunk-> recompute the scores, write the chunk's selected indices in
-//                          ascending order;
-//       2. attention splits: reused units, persistent units, then missed units in layer
-//          order.
-//     score[t] = sum_g (128 - popc(qcode_g ^ kcode_t)) (HATA hash scorer, "CLO
-//     (2511.14510) - L3 Per-Paper Synthesis", section 3.2); k = 10 % of the context
-//     (section 2.2); out_g = sum_r softmax_r(q_g . k_r / sqrt(d)) v_r over the rows.
+// Each CTA holds one fetch warp and one 4-warp compute group (3 CTAs per SM).
+//   * The compute group takes items from one queue, in this order (each list in layer
+//     order, the chunks of a unit next to each other):
+//       1. selection chunks of the missed units (their fetch waits for them);
+//       2. selection of the persistent units (whole units when they fit one group's
+//          shared memory, else chunks);
+//       3. attention splits of the reused units, then of the persistent units, then of
+//          the missed units.
+//     A selection scores every cached token, score[t] = sum_g (128 - popc(qcode_g ^
+//     kcode_t)) (HATA hash scorer, "CLO (2511.14510) - L3 Per-Paper Synthesis", section
+//     3.2), and keeps the k = 10 % best (section 2.2), ties to the lowest index, in
+//     ascending order: a one-digit radix select over the <= 128 G + 1 score values.
+//     An attention split feeds 16-row chunks of K|V rows to each warp through a
+//     shared-memory ring filled by bulk copies on the TMA engine (one 4 d-byte row per
+//     copy, from the unit's cache slot or, for persistent units, gathered from its
+//     resident copy), computes out_g = sum_r softmax_r(q_g . k_r / sqrt(d)) v_r with
+//     tensor-core tiles, and merges partials by log-sum-exp.
 //   * Fetch warps copy the selected K|V rows of missed units from pinned host memory
-//     into the units' on-GPU cache slots with 16-byte loads, chunk by chunk in layer
-//     order, and release one ready flag per chunk (CLO abstract, feature (3):
-//     zero-copy transfer engine and GPU-centric synchronisation; the fetch runs
-//     ahead of the attention that consumes it, as CLO prefetches a layer ahead,
-//     section 5.6).
+//     into the units' on-GPU cache slots with 16-byte loads, 256-row chunk by chunk in
+//     layer order, and release one ready flag per chunk (CLO abstract, feature (3):
+//     zero-copy transfer engine and GPU-centric synchronisation; the fetch runs ahead of
+//     the attention that consumes it, as CLO prefetches a layer ahead, section 5.6).
 // Every wait targets work that sits earlier in the compute queue (or a fetch, which
-// itself waits only on earlier compute items), so the waits form no cycle; each
-// wait is bounded by the context's timeout and reports CLO_ERR_TIMEOUT.
+// itself waits only on earlier compute items), so the waits form no cycle; each wait is
+// bounded by the context's timeout and reports CLO_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <stdlib.h>
 
@@ -41,7 +41,7 @@ namespace {
 constexpr int kCompWarps = 4;
 constexpr int kCompThreads = 32 * kCompWarps;
 constexpr int kFetchUnroll = 4;
-static_assert(kCompWarps == kPartsPerSplit, "one attention partial per compute warp");
+constexpr int kAttStages = 2;  // ring stages of 16 rows per compute warp
 
 __device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
 
@@ -75,10 +75,10 @@ __device__ void wait_flag(const uint32_t* flag, uint32_t target, const DevState&
   }
 }
 
-template <int D, int NBUF>
+template <int D>
 struct AttSmem {
-  static constexpr int ROWW = 2 * D + 8;     // bf16 per smem row (K | V), padded by 16 bytes
-  uint16_t rows[kCompWarps][NBUF][16][ROWW];  // 16-row chunks per warp (NBUF = 2: double buffer)
+  static constexpr int ROWW = 2 * D + 8;             // bf16 per smem row (K | V), padded by 16 bytes
+  uint16_t rows[kCompWarps][kAttStages][16][ROWW];   // each warp's ring of 16-row stages
   float red[kCompWarps];
   int last;
 };
@@ -99,9 +99,9 @@ struct SelUnitSmem {
   int misc[8];
 };
 
-template <int D, int NBUF>
+template <int D>
 union CompSmem {
-  AttSmem<D, NBUF> att;
+  AttSmem<D> att;
   SelSmem sel;
   SelUnitSmem unit;
 };
@@ -222,7 +222,7 @@ template <int G>
 __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int CH, int NC, int gtid) {
   constexpr int NB = 128 * G + 1;
   constexpr int kU = 8;                          // code loads in flight per lane
-  const int WSEG = CH / kCompWarps;              // tokens per warp (CH: 8192 or 16384), a multiple of 32 * kU
+  const int WSEG = CH / kCompWarps;              // tokens per warp (CH: 1024 .. 16384), a multiple of 32 * kU
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
   const int k = s.kcount[b];
@@ -536,16 +536,19 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
 
 // ---- attention split -----------------------------------------------------------------
 // Tensor-core (mma.sync m16n8k16, bf16 in, fp32 accumulate) split attention.  A split
-// is kSplitRows = 1024 selected rows; each of the 4 warps takes 256 of them in
-// double-buffered chunks of 16 (the next chunk's copy overlaps this chunk's math):
+// is kSplitRows = 1024 selected rows; each of the 4 warps takes 256 of them in chunks of
+// 16 rows fed through its own 2-stage ring in shared memory: every row of a chunk is one
+// 512-byte (d = 128) bulk copy on the TMA engine, issued by one lane and counted on the
+// stage's mbarrier, so the next chunk's rows land while this chunk's math runs.  Per
+// chunk:
 //   S[16 rows x 8 heads] = K[16 x d] . Q^T[d x 8]      (G <= 8 query heads of the group
 //                                                         on N; q fragments in registers)
 //   online softmax per head on the accumulator fragments (scores in log2 units)
 //   O^T[d x 8] += V^T[d x 16] . P^T[16 x 8]            (V^T via ldmatrix.trans; P split
 //                                                         into bf16 hi + lo halves, so the
 //                                                         weights keep ~16 mantissa bits)
-// Each warp writes its partial {m, l, acc[d]} per head; the last split of the unit
-// merges all partials by log-sum-exp.
+// At the end of the split the 4 warps' {m, l, acc[d]} are merged in shared memory into one
+// partial per split; the last split of the unit merges those by log-sum-exp.
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, const uint32_t* b) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -566,12 +569,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, const void* p) {
                : "r"(smem_u32(p)));
 }
 
-// 16-byte async copy; src_bytes = 0 fills the destination with zeros.
-__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(src_bytes)
-               : "memory");
-}
-
 // bf16 pair (lo element in the low half) of two floats, round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
@@ -580,12 +577,101 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-template <int D, int NBUF>
-__device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint16_t* __restrict__ q,
-                             float* __restrict__ out, int64_t u, int split, int gtid) {
-  constexpr int VPR = D / 4;  // 16-byte vectors per K|V record
+// Running softmax state of one warp: heads 2*tig and 2*tig+1 (m = max score in log2
+// units, l = sum of weights) and O^T fragments acc[m-block][4].
+template <int D>
+struct AttAcc {
+  float m0, m1, l0, l1;
+  float acc[D / 16][4];
+};
+
+// One 16-row chunk (rows[r][0..D) = K row, rows[r][D..2D) = V row; rows >= nrows hold
+// finite values and are masked).
+template <int D, int ROWW>
+__device__ __forceinline__ void chunk_math(const uint16_t (*rows)[ROWW], int nrows, const uint32_t (*qb)[2],
+                                           float qscale, AttAcc<D>& A, int lane) {
   constexpr int KS = D / 16;  // k-steps of S = K Q^T, also m-blocks of O^T
+  const int gid = lane >> 2, tig = lane & 3;
+  float sf[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ac = 8 * (lane >> 4);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(a, &rows[ar][ks * 16 + ac]);
+      mma_bf16_16816(sf, a, qb[ks]);
+    }
+  }
+  // rows gid (sf[0], sf[1]) and gid + 8 (sf[2], sf[3]); heads 2*tig, 2*tig+1
+  const float s00 = gid < nrows ? sf[0] * qscale : -INFINITY;
+  const float s01 = gid < nrows ? sf[1] * qscale : -INFINITY;
+  const float s10 = gid + 8 < nrows ? sf[2] * qscale : -INFINITY;
+  const float s11 = gid + 8 < nrows ? sf[3] * qscale : -INFINITY;
+  float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(A.m0, mx0), mn1 = fmaxf(A.m1, mx1);
+  const float al0 = exp2f(A.m0 - mn0), al1 = exp2f(A.m1 - mn1);
+  const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
+  const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
+  float rs0 = p00 + p10, rs1 = p01 + p11;
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    rs0 += __shfl_xor_sync(0xffffffffu, rs0, o);
+    rs1 += __shfl_xor_sync(0xffffffffu, rs1, o);
+  }
+  A.l0 = A.l0 * al0 + rs0;
+  A.l1 = A.l1 * al1 + rs1;
+  A.m0 = mn0;
+  A.m1 = mn1;
+#pragma unroll
+  for (int mb = 0; mb < KS; ++mb) {
+    A.acc[mb][0] *= al0;
+    A.acc[mb][2] *= al0;
+    A.acc[mb][1] *= al1;
+    A.acc[mb][3] *= al1;
+  }
+  // P^T fragments (B operand): rows 2*tig, 2*tig+1, 2*tig+8, 2*tig+9 of head gid.
+  // P[r][hd] sits in lane 4*(r%8) + hd/2: element hd%2 of (p00,p01) for r < 8, of
+  // (p10,p11) for r >= 8.
+  const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
+  const bool odd = gid & 1;
+  const float xa0 = __shfl_sync(0xffffffffu, p00, sa), xa1 = __shfl_sync(0xffffffffu, p01, sa);
+  const float xb0 = __shfl_sync(0xffffffffu, p00, sb), xb1 = __shfl_sync(0xffffffffu, p01, sb);
+  const float ya0 = __shfl_sync(0xffffffffu, p10, sa), ya1 = __shfl_sync(0xffffffffu, p11, sa);
+  const float yb0 = __shfl_sync(0xffffffffu, p10, sb), yb1 = __shfl_sync(0xffffffffu, p11, sb);
+  const float pr0 = odd ? xa1 : xa0, pr1 = odd ? xb1 : xb0;  // rows 2*tig, 2*tig+1
+  const float pr8 = odd ? ya1 : ya0, pr9 = odd ? yb1 : yb0;  // rows 2*tig+8, 2*tig+9
+  uint32_t bh[2], bl[2];
+  bh[0] = pack_bf16(pr0, pr1);
+  bh[1] = pack_bf16(pr8, pr9);
+  bl[0] = pack_bf16(pr0 - bf16_round(pr0), pr1 - bf16_round(pr1));
+  bl[1] = pack_bf16(pr8 - bf16_round(pr8), pr9 - bf16_round(pr9));
+  // O^T += V^T P^T
+  {
+    const int vr = (lane & 7) + 8 * (lane >> 4), vc = 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int mb = 0; mb < KS; ++mb) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, &rows[vr][D + mb * 16 + vc]);
+      mma_bf16_16816(A.acc[mb], a, bh);
+      mma_bf16_16816(A.acc[mb], a, bl);
+    }
+  }
+}
+
+// bars: this warp's kAttStages mbarriers (one per ring stage); phase: bit st = parity of
+// the next completion of stage st, carried across items.
+template <int D>
+__device__ void attend_split(const DevState& s, AttSmem<D>& sm, uint64_t* bars, uint32_t& phase,
+                             const uint16_t* __restrict__ q, float* __restrict__ out, int64_t u, int split,
+                             int gtid) {
+  constexpr int ROWW = AttSmem<D>::ROWW;
   constexpr int WROWS = kSplitRows / kCompWarps;
+  constexpr int ST = kAttStages;
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
   const int l = (int)(u / ((int64_t)s.Hkv * s.B));
@@ -595,21 +681,55 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
   const int64_t k = s.kcount[b];
   const int64_t r0 = (int64_t)split * kSplitRows + (int64_t)warp * WROWS;
   const int64_t r1 = (r0 + WROWS < k) ? r0 + WROWS : k;
+  const int nch = r1 > r0 ? (int)((r1 - r0 + 15) / 16) : 0;
   const bool persistent = s.decision[u] == CLO_DEC_PERSIST;
   const int32_t* ix = s.idx + u * s.kmax;
-  const uint4* src;
+  const uint16_t* src;
   if (persistent) {
     const int p = s.persist_slot[l * s.Hkv + h];
-    src = reinterpret_cast<const uint4*>(s.resident) + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax) * VPR;
+    src = s.resident + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax) * (2 * D);
   } else {
-    src = reinterpret_cast<const uint4*>(s.slots) + (u * s.kmax) * VPR;
+    src = s.slots + (u * s.kmax) * (2 * D);
+  }
+  // source row of lane's row (lane < 16) in chunk c: persistent units read their rows
+  // through the selection's indices, loaded one chunk ahead of the copy that needs them
+  auto row_of = [&](int c) -> int64_t {
+    const int64_t t = r0 + 16 * c + lane;
+    if (lane >= 16 || c >= nch || t >= r1) return -1;
+    if (!persistent) return t;
+    const int64_t v = __ldcg(ix + t);
+    if (v < 0 || v >= N) {
+      atomicOr(s.err, kErrBounds);
+      return 0;
+    }
+    return v;
+  };
+  auto issue = [&](int c, int64_t row) {
+    const int st = c % ST;
+    const int nr = (int)((r1 - (r0 + 16 * c)) < 16 ? (r1 - (r0 + 16 * c)) : 16);
+    fence_proxy_async_smem();  // this warp's earlier generic accesses of the stage first
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)nr * 4 * D);
+    __syncwarp();
+    if (lane < nr) {
+      bulk_copy_g2s(&sm.rows[warp][st][lane][0], src + row * (2 * D), 4 * D, &bars[st]);
+    } else if (lane < 16) {  // rows past the end: zeros, so the masked rows stay finite
+      uint4* z = reinterpret_cast<uint4*>(&sm.rows[warp][st][lane][0]);
+#pragma unroll 4
+      for (int e = 0; e < ROWW / 8; ++e) z[e] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  int64_t nxt = row_of(0);
+  for (int c = 0; c < ST - 1 && c < nch; ++c) {
+    issue(c, nxt);
+    nxt = row_of(c + 1);
   }
   // Q^T fragments (B operand): head gid, dims 2*tig (+1, +8, +9) of each k-step
-  uint32_t qb[KS][2];
+  uint32_t qb[D / 16][2];
   {
     const uint16_t* qg = q + (((int64_t)(l - s.q_l0) * s.B + b) * s.Hq + (int64_t)h * G) * D;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
+    for (int ks = 0; ks < D / 16; ++ks) {
       if (gid < G) {
         qb[ks][0] = *reinterpret_cast<const uint32_t*>(qg + gid * D + ks * 16 + 2 * tig);
         qb[ks][1] = *reinterpret_cast<const uint32_t*>(qg + gid * D + ks * 16 + 2 * tig + 8);
@@ -619,170 +739,76 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
     }
   }
   const float qscale = 1.4426950408889634f * rsqrtf((float)D);  // scores in log2 units
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;      // heads 2*tig, 2*tig+1
-  float acc[KS][4];
+  AttAcc<D> A;
+  A.m0 = A.m1 = -INFINITY;
+  A.l0 = A.l1 = 0.f;
 #pragma unroll
-  for (int mb = 0; mb < KS; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
-
-  // copy layout: lane -> row lane % 16, half lane / 16 of the record's vectors
-  const int cr = lane & 15, chalf = lane >> 4;
-  auto row_of = [&](int64_t rb) -> int64_t {
-    const int64_t t = rb + cr;
-    if (t >= r1) return 0;
-    if (!persistent) return t;
-    int64_t v = __ldcg(ix + t);
-    if (v < 0 || v >= N) {
-      atomicOr(s.err, kErrBounds);
-      v = 0;
+  for (int mb = 0; mb < D / 16; ++mb) A.acc[mb][0] = A.acc[mb][1] = A.acc[mb][2] = A.acc[mb][3] = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    if (c + ST - 1 < nch) {
+      issue(c + ST - 1, nxt);
+      nxt = row_of(c + ST);
     }
-    return v;
-  };
-  auto issue = [&](int64_t rb, int buf, int64_t srow) {
-    const uint32_t bytes = rb + cr < r1 ? 16u : 0u;
-    const uint4* sp = src + srow * VPR + chalf * (VPR / 2);
-    uint16_t* dp = &sm.rows[warp][buf][cr][chalf * (VPR / 2) * 8];
-#pragma unroll
-    for (int c = 0; c < VPR / 2; ++c) cp_async16_zfill(dp + c * 8, sp + c, bytes);
-    cp_async_commit();
-  };
-  // L2 prefetch of the rows kPf chunks ahead (lane < 16: one row each), so the copies
-  // into shared memory find them in L2: more reads in flight than the two row buffers hold
-  constexpr int kPf = 4;
-  auto pf_row_of = [&](int64_t rb) -> int64_t {  // source row of lane's row in chunk rb, or -1
-    const int64_t t = rb + (lane & 15);
-    if (lane >= 16 || t >= r1) return -1;
-    if (!persistent) return t;
-    const int64_t v = __ldcg(ix + t);
-    return (v < 0 || v >= N) ? -1 : v;
-  };
-  if (r0 < r1) {
-    for (int c = 2; c < kPf; ++c) {
-      const int64_t pr = pf_row_of(r0 + 16 * c);
-      if (pr >= 0) prefetch_l2(src + pr * VPR, 16u * VPR);
-    }
-    int64_t pf = pf_row_of(r0 + 16 * kPf);
-    int64_t nxt = row_of(r0);
-    if (NBUF == 2) {
-      issue(r0, 0, nxt);
-      nxt = row_of(r0 + 16);
-    }
-    int ci = 0;
-    for (int64_t rb = r0; rb < r1; rb += 16, ++ci) {
-      const int buf = NBUF == 2 ? (ci & 1) : 0;
-      if (pf >= 0) prefetch_l2(src + pf * VPR, 16u * VPR);
-      pf = pf_row_of(rb + 16 * (kPf + 1));
-      if (NBUF == 2) {
-        if (rb + 16 < r1) {
-          issue(rb + 16, buf ^ 1, nxt);
-          nxt = row_of(rb + 32);
-          cp_async_wait<1>();
-        } else {
-          cp_async_wait<0>();
-        }
-      } else {
-        issue(rb, 0, nxt);
-        nxt = row_of(rb + 16);  // index load overlaps the copy
-        cp_async_wait<0>();
-      }
-      __syncwarp();
-      uint16_t(*rows)[AttSmem<D, NBUF>::ROWW] = sm.rows[warp][buf];
-      const int nrows = (int)((r1 - rb) < 16 ? (r1 - rb) : 16);
-      // S = K Q^T
-      float sf[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const int ar = (lane & 7) + 8 * ((lane >> 3) & 1), ac = 8 * (lane >> 4);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a[4];
-          ldsm_x4(a, &rows[ar][ks * 16 + ac]);
-          mma_bf16_16816(sf, a, qb[ks]);
-        }
-      }
-      // rows gid (sf[0], sf[1]) and gid + 8 (sf[2], sf[3]); heads 2*tig, 2*tig+1
-      const float s00 = gid < nrows ? sf[0] * qscale : -INFINITY;
-      const float s01 = gid < nrows ? sf[1] * qscale : -INFINITY;
-      const float s10 = gid + 8 < nrows ? sf[2] * qscale : -INFINITY;
-      const float s11 = gid + 8 < nrows ? sf[3] * qscale : -INFINITY;
-      float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      const float p00 = exp2f(s00 - mn0), p10 = exp2f(s10 - mn0);
-      const float p01 = exp2f(s01 - mn1), p11 = exp2f(s11 - mn1);
-      float rs0 = p00 + p10, rs1 = p01 + p11;
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        rs0 += __shfl_xor_sync(0xffffffffu, rs0, o);
-        rs1 += __shfl_xor_sync(0xffffffffu, rs1, o);
-      }
-      l0 = l0 * al0 + rs0;
-      l1 = l1 * al1 + rs1;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mb = 0; mb < KS; ++mb) {
-        acc[mb][0] *= al0;
-        acc[mb][2] *= al0;
-        acc[mb][1] *= al1;
-        acc[mb][3] *= al1;
-      }
-      // P^T fragments (B operand): rows 2*tig, 2*tig+1, 2*tig+8, 2*tig+9 of head gid.
-      // P[r][hd] sits in lane 4*(r%8) + hd/2: element hd%2 of (p00,p01) for r < 8, of
-      // (p10,p11) for r >= 8.
-      const int sa = 8 * tig + (gid >> 1), sb = sa + 4;
-      const bool odd = gid & 1;
-      const float xa0 = __shfl_sync(0xffffffffu, p00, sa), xa1 = __shfl_sync(0xffffffffu, p01, sa);
-      const float xb0 = __shfl_sync(0xffffffffu, p00, sb), xb1 = __shfl_sync(0xffffffffu, p01, sb);
-      const float ya0 = __shfl_sync(0xffffffffu, p10, sa), ya1 = __shfl_sync(0xffffffffu, p11, sa);
-      const float yb0 = __shfl_sync(0xffffffffu, p10, sb), yb1 = __shfl_sync(0xffffffffu, p11, sb);
-      const float pr0 = odd ? xa1 : xa0, pr1 = odd ? xb1 : xb0;  // rows 2*tig, 2*tig+1
-      const float pr8 = odd ? ya1 : ya0, pr9 = odd ? yb1 : yb0;  // rows 2*tig+8, 2*tig+9
-      uint32_t bh[2], bl[2];
-      bh[0] = pack_bf16(pr0, pr1);
-      bh[1] = pack_bf16(pr8, pr9);
-      bl[0] = pack_bf16(pr0 - bf16_round(pr0), pr1 - bf16_round(pr1));
-      bl[1] = pack_bf16(pr8 - bf16_round(pr8), pr9 - bf16_round(pr9));
-      // O^T += V^T P^T
-      {
-        const int vr = (lane & 7) + 8 * (lane >> 4), vc = 8 * ((lane >> 3) & 1);
-#pragma unroll
-        for (int mb = 0; mb < KS; ++mb) {
-          uint32_t a[4];
-          ldsm_x4_trans(a, &rows[vr][D + mb * 16 + vc]);
-          mma_bf16_16816(acc[mb], a, bh);
-          mma_bf16_16816(acc[mb], a, bl);
-        }
-      }
-      __syncwarp();  // this buffer is refilled by a later chunk
-    }
+    const int st = c % ST;
+    const uint32_t par = (phase >> st) & 1u;
+    bool ok = mbar_wait_bounded(&bars[st], par, s.err, (uint64_t)s.wait_timeout_ns);
+    if (!ok) ok = mbar_wait_bounded(&bars[st], par, s.err, (uint64_t)s.wait_timeout_ns);  // drain
+    phase ^= 1u << st;
+    const int nrows = (int)((r1 - (r0 + 16 * c)) < 16 ? (r1 - (r0 + 16 * c)) : 16);
+    if (ok) chunk_math<D, ROWW>(sm.rows[warp][st], nrows, qb, qscale, A, lane);
+    __syncwarp();  // the stage is refilled by a later chunk
   }
 
-  // this warp's partial: {m, l, acc[d]} for heads 2*tig, 2*tig+1 (< G)
-  float* part = s.part + (((u * s.nsplit + split) * kCompWarps + warp) * G) * (D + 2);
-  const int h0 = 2 * tig, h1 = 2 * tig + 1;
+  // the warp's partial {m, l, acc[d]} per head into its own ring region (its copies are
+  // all complete): wp[g][D + 2]
+  float* wp = reinterpret_cast<float*>(&sm.rows[warp][0][0][0]);
+  {
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
 #pragma unroll
-  for (int mb = 0; mb < KS; ++mb) {
-    if (h0 < G) {
-      part[h0 * (D + 2) + 2 + mb * 16 + gid] = acc[mb][0];
-      part[h0 * (D + 2) + 2 + mb * 16 + gid + 8] = acc[mb][2];
+    for (int mb = 0; mb < D / 16; ++mb) {
+      if (h0 < G) {
+        wp[h0 * (D + 2) + 2 + mb * 16 + gid] = A.acc[mb][0];
+        wp[h0 * (D + 2) + 2 + mb * 16 + gid + 8] = A.acc[mb][2];
+      }
+      if (h1 < G) {
+        wp[h1 * (D + 2) + 2 + mb * 16 + gid] = A.acc[mb][1];
+        wp[h1 * (D + 2) + 2 + mb * 16 + gid + 8] = A.acc[mb][3];
+      }
     }
-    if (h1 < G) {
-      part[h1 * (D + 2) + 2 + mb * 16 + gid] = acc[mb][1];
-      part[h1 * (D + 2) + 2 + mb * 16 + gid + 8] = acc[mb][3];
+    if (gid == 0) {
+      if (h0 < G) {
+        wp[h0 * (D + 2) + 0] = A.m0;
+        wp[h0 * (D + 2) + 1] = A.l0;
+      }
+      if (h1 < G) {
+        wp[h1 * (D + 2) + 0] = A.m1;
+        wp[h1 * (D + 2) + 1] = A.l1;
+      }
     }
   }
-  if (gid == 0) {
-    if (h0 < G) {
-      part[h0 * (D + 2) + 0] = m0;
-      part[h0 * (D + 2) + 1] = l0;
-    }
-    if (h1 < G) {
-      part[h1 * (D + 2) + 0] = m1;
-      part[h1 * (D + 2) + 1] = l1;
+  comp_bar();
+  // the split's partial: the 4 warps merged by log-sum-exp (a warp without rows has l = 0)
+  {
+    float* part = s.part + ((u * s.nsplit + split) * G) * (D + 2);
+    const float* w0 = reinterpret_cast<const float*>(&sm.rows[0][0][0][0]);
+    constexpr int WSTRIDE = (int)(sizeof(sm.rows[0]) / sizeof(float));
+    for (int e = gtid; e < G * (D + 2); e += kCompThreads) {
+      const int g = e / (D + 2), j = e % (D + 2);
+      float mw[kCompWarps], lw[kCompWarps];
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kCompWarps; ++w) {
+        mw[w] = w0[w * WSTRIDE + g * (D + 2)];
+        lw[w] = w0[w * WSTRIDE + g * (D + 2) + 1];
+        if (lw[w] > 0.f) M = fmaxf(M, mw[w]);
+      }
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCompWarps; ++w) {
+        const float sc = lw[w] > 0.f ? exp2f(mw[w] - M) : 0.f;
+        v = fmaf(j == 1 ? lw[w] : w0[w * WSTRIDE + g * (D + 2) + j], sc, v);
+      }
+      part[e] = j == 0 ? M : v;
     }
   }
   __threadfence();
@@ -794,9 +820,9 @@ __device__ void attend_split(const DevState& s, AttSmem<D, NBUF>& sm, const uint
   comp_bar();
   if (!sm.last) return;
   __threadfence();
-  // merge: per head, weights w_sp = exp2(m_sp - M) of all partials (into shared memory,
-  // reusing the row buffers), then out[j] = sum_sp w_sp acc_sp[j] / sum_sp w_sp l_sp
-  const int np = s.nsplit * kCompWarps;
+  // merge: per head, weights w_sp = exp2(m_sp - M) of the splits' partials (into shared
+  // memory), then out[j] = sum_sp w_sp acc_sp[j] / sum_sp w_sp l_sp
+  const int np = s.nsplit;
   const float* pu = s.part + (u * np) * G * (D + 2);
   float* og = out + (((int64_t)(l - s.q_l0) * s.B + b) * s.Hq + (int64_t)h * G) * D;
   float* w = reinterpret_cast<float*>(&sm.rows[0][0][0][0]);  // np floats
@@ -904,23 +930,31 @@ __device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_
   }
 }
 
+// A fetch item is fetch_rows (256, 128, 64 or 32) rows of one chunk of kChunkRows; every
+// item of a chunk (empty ones too) adds 1 to the chunk's ready flag, which is complete at
+// kChunkRows / fetch_rows.  Launches with few missed rows use small items, so the rows
+// of a layer are spread over many fetch warps.
 template <int D, int FU>
 __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int lane, int32_t* sidx) {
   constexpr int kFetchUnroll = FU;
-  const int NS = s.nchunk, RS = kChunkRows, L = s.L, BH = s.B * s.Hkv;
-  const int64_t n_items = (int64_t)n_miss * NS;
+  const int NS = s.nchunk, L = s.L, BH = s.B * s.Hkv;
+  const int RS = s.fetch_rows, SUB = kChunkRows / RS;
+  const int64_t per_unit = (int64_t)NS * SUB;
+  const int64_t n_items = (int64_t)n_miss * per_unit;
   while (true) {
     unsigned item = 0;
     if (lane == 0) item = atomicAdd(&s.queue[0], 1u);
     item = __shfl_sync(0xffffffffu, item, 0);
     if ((int64_t)item >= n_items) break;
-    const int p = (int)(item / NS), c = (int)(item % NS);
+    const int p = (int)(item / per_unit);
+    const int rest = (int)(item % per_unit);
+    const int c = rest / SUB;
     const int l = layer_of(pre_m, L, p);
     const int64_t u = s.miss_list[(int64_t)l * BH + (p - pre_m[l])];
     const int b = (int)((u / s.Hkv) % s.B);
     const int64_t k = s.kcount[b];
     const int64_t N = s.ntok[b];
-    const int64_t r0 = (int64_t)c * RS;
+    const int64_t r0 = (int64_t)c * kChunkRows + (int64_t)(rest % SUB) * RS;
     const int nr = (int)((r0 + RS < k) ? RS : (k - r0 > 0 ? k - r0 : 0));
     if (nr > 0) {
       if (lane == 0) {  // the unit's selection: compute groups, earlier in their queue
@@ -958,17 +992,19 @@ __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int 
 }
 
 // ---- the kernel ------------------------------------------------------------------------
-// FW fetch warps + one compute group per CTA; MINB CTAs per SM; NBUF row buffers per
-// compute warp.
-template <int D, int G, int FW, int MINB, int NBUF, int FU = kFetchUnroll>
+// FW fetch warps + one compute group per CTA; MINB CTAs per SM.
+template <int D, int G, int FW, int MINB, int FU = kFetchUnroll>
 __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     k_step_fused(DevState s, const uint16_t* __restrict__ q, float* __restrict__ out) {
-  using Smem = CompSmem<D, NBUF>;
+  using Smem = CompSmem<D>;
   __shared__ int pre[3][kMaxLayers + 1];  // hit, persistent, missed lists
   __shared__ long long sec_start[6];
   __shared__ int s_item;
   __shared__ unsigned long long s_t0, s_t1;  // start of the group's item, end of its waits (timing mode)
   __shared__ int32_t fidx[FW][kChunkRows];
+  // mbarriers of the compute warps' row rings (outside the union: selection items reuse
+  // the ring memory, never the barriers)
+  __shared__ __align__(8) uint64_t att_bar[kCompWarps][kAttStages];
   extern __shared__ __align__(128) unsigned char dsm[];
   Smem& sm = *reinterpret_cast<Smem*>(dsm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1013,6 +1049,10 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
   const int BH = s.B * s.Hkv;
   const int NC = s.nch;
   const long long total = sec_start[5];
+  if (lane < kAttStages) mbar_init(&att_bar[gtid >> 5][lane], 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+  uint32_t att_phase = 0;  // bit st: parity of the next completion of this warp's stage st
   while (true) {
     if (gtid == 0) s_item = (int)atomicAdd(&s.queue[1], 1u);
     comp_bar();
@@ -1055,14 +1095,15 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
       } else if (sec == 4 && r0 < s.kcount[b]) {
         if (gtid == 0) {
           constexpr int kPer = kSplitRows / kChunkRows;  // the fetch chunks this split reads
+          const uint32_t subs = (uint32_t)(kChunkRows / s.fetch_rows);  // fetch items per chunk
           for (int fc = c * kPer; fc < (c + 1) * kPer && (int64_t)fc * kChunkRows < s.kcount[b]; ++fc)
-            wait_flag(&s.ready[u * s.nchunk + fc], 1u, s);
+            wait_flag(&s.ready[u * s.nchunk + fc], subs, s);
           if (s.timeline) atomicAdd(&s.timeline[TL_ATT_WAIT_NS], global_timer_ns() - s_t0);
         }
         comp_bar();
       }
       if (s.timeline && gtid == 0) s_t1 = global_timer_ns();
-      attend_split<D, NBUF>(s, sm.att, q, out, u, c, gtid);
+      attend_split<D>(s, sm.att, att_bar[gtid >> 5], att_phase, q, out, u, c, gtid);
       if (s.timeline && gtid == 0) {
         const uint64_t t1 = global_timer_ns();
         atomicMax(&s.timeline[TL_COMP_END], t1);
@@ -1071,16 +1112,19 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
         atomicAdd(&s.timeline[TL_ATT_ITEMS], 1ull);
       }
     }
+    // this item's generic shared-memory accesses happen before any later bulk copy into
+    // the same memory (the copies are issued after the next comp_bar)
+    fence_proxy_async_smem();
     comp_bar();
   }
 }
 
-template <int D, int G, int FW, int MINB, int NBUF, int FU>
+template <int D, int G, int FW, int MINB, int FU>
 int fused_grid() {
   static int grid = 0;
   if (grid == 0) {
-    auto kern = k_step_fused<D, G, FW, MINB, NBUF, FU>;
-    const int smem = (int)sizeof(CompSmem<D, NBUF>);
+    auto kern = k_step_fused<D, G, FW, MINB, FU>;
+    const int smem = (int)sizeof(CompSmem<D>);
     int dev = 0, sms = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1091,10 +1135,10 @@ int fused_grid() {
   return grid;
 }
 
-template <int D, int G, int FW, int MINB, int NBUF, int FU = kFetchUnroll>
+template <int D, int G, int FW, int MINB, int FU = kFetchUnroll>
 cudaError_t launch_v(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
-  k_step_fused<D, G, FW, MINB, NBUF, FU><<<fused_grid<D, G, FW, MINB, NBUF, FU>(), 32 * (FW + kCompWarps),
-                                       sizeof(CompSmem<D, NBUF>), st>>>(s, q, out);
+  k_step_fused<D, G, FW, MINB, FU><<<fused_grid<D, G, FW, MINB, FU>(), 32 * (FW + kCompWarps),
+                                   sizeof(CompSmem<D>), st>>>(s, q, out);
   return cudaGetLastError();
 }
 
@@ -1102,8 +1146,8 @@ template <int D, int G>
 cudaError_t launch_dg(const DevState& s, const uint16_t* q, float* out, cudaStream_t st) {
   // the selection's waits need all chunks of a unit running at once
   const int nc = s.nch > s.nch_miss ? s.nch : s.nch_miss;
-  if (fused_grid<D, G, 1, 3, 2, kFetchUnroll>() < nc) return cudaErrorInvalidConfiguration;
-  return launch_v<D, G, 1, 3, 2>(s, q, out, st);
+  if (fused_grid<D, G, 1, 3, kFetchUnroll>() < nc) return cudaErrorInvalidConfiguration;
+  return launch_v<D, G, 1, 3>(s, q, out, st);
 }
 
 template <int D>

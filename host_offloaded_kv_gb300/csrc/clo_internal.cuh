@@ -70,9 +70,10 @@ struct DevState {
   unsigned long long* total_ctr;// [C_NUM][kCtrLanes] since init
   uint32_t* err;                // error word
   uint32_t* unit_done;          // [U] split counters of the attention combine
-  float* part;                  // attention partials [U][nsplit][kPartsPerSplit][G][d + 2]
+  float* part;                  // attention partials [U][nsplit][G][d + 2] (one per split)
   int nsplit;                   // attention splits per unit (kSplitRows rows each)
   int nchunk;                   // fetch chunks per unit (kChunkRows rows each)
+  int fetch_rows;               // rows per fetch item: 256, 128, 64 or 32 (divides kChunkRows)
   uint32_t* ready;              // [U][nchunk] fetch-ready flag per row chunk (zeroed per step)
   int* lcnt;                    // [3L] per-layer list lengths: hit, persistent, missed (zeroed per step)
   int32_t* hit_list;            // [L][B*Hkv] units reusing their selection, per layer
@@ -129,8 +130,8 @@ enum Timeline : int {
   TL_ATT_RUN_NS = 15,    // summed durations of attention splits after their waits
   kTimelineSlots = 16
 };
-constexpr int kSelChunkMax = 16384;  // tokens per selection chunk, at most (8192 or 16384)
-constexpr int kPartsPerSplit = 4; // attention partials per split (one per compute warp)
+constexpr int kSelChunkMax = 16384;  // tokens per selection chunk, at most
+constexpr int kSelChunkMin = 1024;   // tokens per selection chunk, at least
 constexpr int kSplitRows = 1024;  // selected rows per attention split
 constexpr int kChunkRows = 256;   // selected rows per fetch chunk (one ready flag each)
 constexpr int kNBPad = 1056;     // >= 128 * kMaxG + 1, multiple of 32

@@ -203,6 +203,11 @@ extern "C" CLO_API clo_status clo_sparse_attention_noalloc(const void* q, const 
   if (n_groups < 1 || group_size < 1 || group_size > kMaxG || (head_dim != 64 && head_dim != 128) || k < 1)
     return fail(CLO_ERR_INVALID, "clo_sparse_attention_noalloc: need n_groups >= 1, 1 <= group_size <= 8, "
                                  "head_dim 64 or 128, k >= 1");
+  // rows are read with 16-byte asynchronous copies, q as bf16 and out as fp32 words
+  if ((reinterpret_cast<uintptr_t>(rows) & 15u) != 0 || (reinterpret_cast<uintptr_t>(q) & 1u) != 0 ||
+      (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+    return fail(CLO_ERR_INVALID, "clo_sparse_attention_noalloc: rows must be 16-byte aligned, q 2-byte and out "
+                                 "4-byte aligned");
   const int64_t nsplit = (k + kNaSplitRows - 1) / kNaSplitRows;
   const int64_t need = (int64_t)n_groups * nsplit * group_size * (head_dim + 2);
   if (n_groups > kNaMaxGroups || need > kNaPartWords)

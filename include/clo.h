@@ -142,7 +142,8 @@ typedef struct clo_stats_t {
  * tau_offset 0.05; wait 2 s; debug_drop_flag_layer -1; adaptive_tau 0, tau_ema 1/16). */
 CLO_API void clo_config_default(clo_config* cfg);
 
-/* Create a context: allocates the pinned, device-mapped host K/V pool
+/* Create a context: allocates the pinned, device-mapped host K/V pool (on a host with
+ * several NUMA nodes, with its pages preferred on the node of the GPU's PCI function)
  * (L*B*Hkv*max_tokens records of K||V, 4*d bytes each, [SYN] 3.4 attack 7 sizes the
  * pool of a 512K Qwen2.5-14B context at 93.75 GB) and the HBM state (hash codes,
  * selections, cache slots, resident copies).  *out receives the context.
@@ -242,6 +243,11 @@ CLO_API const char* clo_last_error(void);
  *                       of attention splits, [12] their number, [13] first CTA of
  *                       the step's decide kernel started, [14] its last CTA finished,
  *                       [15] summed durations of attention splits after their waits
+ *   CLO_DBG_TOPK        int32 [L][B]  top-k count k of each (layer, sequence) at its
+ *                       current length (the rule of clo_config.topk / topk_ratio)
+ *   CLO_DBG_POOL_NODE   int32 [1]     NUMA node the pinned pool's pages were placed on
+ *                       (-1: not placed: a host with one memory node, or placement failed
+ *                       and the pool came from cudaHostAlloc)
  * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,
@@ -253,7 +259,9 @@ enum {
   CLO_DBG_PERSIST = 7,
   CLO_DBG_SHAT = 8,
   CLO_DBG_COS = 9,
-  CLO_DBG_TIMELINE = 10
+  CLO_DBG_TIMELINE = 10,
+  CLO_DBG_TOPK = 11,
+  CLO_DBG_POOL_NODE = 12
 };
 CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int32_t seq, int32_t kvh, void* dst,
                                  int64_t dst_bytes);
@@ -265,16 +273,15 @@ enum { CLO_SET_DROP_FLAG_LAYER = 1, CLO_SET_WAIT_TIMEOUT_NS = 2 };
 CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
 
 /* Split-K sparse decode attention that allocates nothing: the attention over a
- * top-k selection of the decode step ([SYN] 2.2: top-k = 10 % attention) on rows
- * the caller provides.  The paper has no counterpart to this call as an entry
- * point; it is here for callers that are not allowed to
+ * selection of rows the caller provides.  The paper has no counterpart to this
+ * call; it is here for callers that are not allowed to
  * allocate device memory themselves or through the library: a serving engine or
  * plugin host that plans every byte of device memory up front and hands kernels
  * only their inputs and outputs, or a latency-critical loop that cannot take the
  * device-wide stalls cudaMalloc/cudaFree may cause.
  *   q:    device bf16 [n_groups][group_size][head_dim]  (one GQA group per row)
  *   rows: device bf16 [n_groups][k][2][head_dim]         (K row then V row of each
- *         selected token, the layout of the library's cache slots)
+ *         selected token, the layout of the library's cache slots); 16-byte aligned
  *   out:  device fp32 [n_groups][group_size][head_dim], written by the call
  *   out_g = sum_r softmax_r(q_g . K_r / sqrt(head_dim)) V_r over the k rows.
  * group_size <= 8, head_dim 64 or 128, k >= 1.  Work is enqueued on stream
@@ -284,10 +291,13 @@ CLO_API clo_status clo_set(clo_ctx* ctx, int32_t key, int64_t value);
  * beyond it are rejected with CLO_ERR_INVALID: n_groups <= 4096 and
  * n_groups * ceil(k / 256) * group_size * (head_dim + 2) <= 2097152.
  * The first call on a device looks up that array's device address (once per
- * device, with that device current); make the first call before any stream
- * capture.  All calls share the array: calls whose work overlaps on the GPU race
+ * device, with that device current) and keeps it for the life of the process;
+ * make the first call before any stream capture.  The kept address does not
+ * survive cudaDeviceReset() or a rebuilt primary context: do not call this
+ * entry point again in a process after either.  All calls share the array: calls whose work overlaps on the GPU race
  * on it, so serialise them (one stream, or events).  No cudaMalloc, cudaFree or
- * other allocating routine is called.  Errors: CLO_ERR_INVALID, CLO_ERR_CUDA. */
+ * other allocating routine is called.  Errors: CLO_ERR_INVALID (null or misaligned
+ * pointer, sizes), CLO_ERR_CUDA. */
 CLO_API clo_status clo_sparse_attention_noalloc(const void* q, const void* rows, float* out, int32_t n_groups,
                                                 int32_t group_size, int32_t head_dim, int64_t k, void* stream);
 

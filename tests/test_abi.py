@@ -103,3 +103,29 @@ def test_struct_layout_matches_header(libpath):
     sizes = subprocess.run([exe], capture_output=True, text=True).stdout.split()
     assert int(sizes[0]) == ctypes.sizeof(clo.clo_config)
     assert int(sizes[1]) == ctypes.sizeof(clo.clo_stats_t)
+
+
+@pytest.mark.parametrize("q,rows,out", [(0x10000, 0x10008, 0x20000), (0x10001, 0x10000, 0x20000),
+                                        (0x10000, 0x10000, 0x20002)])
+def test_noalloc_refuses_misaligned_pointers_without_gpu(libpath, q, rows, out):
+    # rows are read with 16-byte copies, q as bf16, out as fp32: a misaligned pointer is
+    # refused before any CUDA call (the addresses are never dereferenced)
+    from host_offloaded_kv_gb300 import clo
+
+    lib = clo.load_library()
+    st = lib.clo_sparse_attention_noalloc(q, rows, out, 4, 4, 128, 300, None)
+    assert st == clo.CLO_ERR_INVALID
+    assert "aligned" in clo.clo_last_error()
+
+
+def test_noalloc_python_wrapper_refuses_host_buffers(libpath):
+    from host_offloaded_kv_gb300 import clo
+
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((2, 4, 64), dtype=torch.int16)
+    rows = torch.zeros((2, 10, 2, 64), dtype=torch.int16)
+    out = torch.zeros((2, 4, 64), dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        clo.clo_sparse_attention_noalloc(q, rows, out, 2, 4, 64, 10)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        clo.clo_sparse_attention_noalloc(q.numpy(), rows, out, 2, 4, 64, 10)
