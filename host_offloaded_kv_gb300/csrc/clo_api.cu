@@ -140,8 +140,8 @@ struct clo_ctx {
   int64_t step = 0;
   bool warmup_mode = false;
   int kv_bits = 16;
-  int whole_unit_min_units = 0;  // launches with at least this many units select units whole
   int sms = 0;                   // multiprocessors of the device
+  int whole_unit_min_units = 0;  // launches with at least this many units select persistent units whole
   uint16_t* kstep = nullptr;     // staging of clo_append_step's host rows
   uint16_t* vstep = nullptr;
   int next_layer = 0;  // next layer of a layer-by-layer step (0: none in progress)
@@ -345,17 +345,16 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   }
   // per-step zeroed region: step counters, per-layer list lengths, work queues, ready
   // flags of the fetch chunks, selection progress counters
-  // selection: contexts up to 32K tokens are selected whole by one compute group (the
-  // scores fit in its shared memory); longer ones in chunks of 16384 tokens by several
-  s.sel_chunk = c->Nmax <= 32768 ? (int)c->Nmax : kSelChunkMax;
+  // selection in chunks of 8192 (contexts up to 32K) or 16384 tokens (refined per launch)
+  s.sel_chunk = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
   s.nch = (int)((c->Nmax + s.sel_chunk - 1) / s.sel_chunk);
   s.sel_chunk_miss = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
   s.nch_miss = (int)((c->Nmax + s.sel_chunk_miss - 1) / s.sel_chunk_miss);
-  {  // launches with few units split them into 8192-token chunks (see enqueue_layers)
+  {  // launches with few units use smaller chunks and fetch items (see enqueue_layers)
     int sms = 0;
     CLO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    c->whole_unit_min_units = 4 * sms;
     c->sms = sms;
+    c->whole_unit_min_units = 4 * sms;
   }
   const int nch_max = (int)((c->Nmax + kSelChunkMin - 1) / kSelChunkMin);
   s.nbp = (128 * c->G + 1 + 31) / 32 * 32;
@@ -574,12 +573,6 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   s.l0 = l0;
   s.l1 = l1;
   s.q_l0 = l0;
-  // selection granularity: a context of up to 32K tokens is selected whole by one compute
-  // group when the launch has units enough to occupy the groups; otherwise (one layer
-  // of a layer-by-layer step, small batches) in chunks of 8192 tokens by several
-  // groups, which selects each unit sooner
-  // (missed units always use chunks: their fetch waits for the selection, and chunks
-  // select a unit sooner)
   const int64_t units = (int64_t)(l1 - l0) * c->B * c->Hkv;
   // chunks of 8192 (contexts up to 32K) or 16384 tokens, halved (down to 1024) while the
   // launch's units would give fewer than 4 chunks per SM: a launch with few units (one
@@ -589,6 +582,8 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   auto nchunks = [&](int ch) { return (c->Nmax + ch - 1) / ch; };
   while (chunk > kSelChunkMin && units * nchunks(chunk) < 4LL * c->sms && nchunks(chunk / 2) <= c->sms) chunk /= 2;
   s.sel_chunk_miss = chunk;
+  // persistent units of contexts up to 32K are selected whole by one group (no waits on
+  // other groups) when the launch holds units enough to occupy the groups
   s.sel_chunk = (c->Nmax <= 32768 && units >= c->whole_unit_min_units) ? (int)c->Nmax : chunk;
   s.nch = (int)nchunks(s.sel_chunk);
   s.nch_miss = (int)nchunks(s.sel_chunk_miss);

@@ -8,8 +8,8 @@
 //   * The compute group takes items from one queue, in this order (each list in layer
 //     order, the chunks of a unit next to each other):
 //       1. selection chunks of the missed units (their fetch waits for them);
-//       2. selection of the persistent units (whole units when they fit one group's
-//          shared memory, else chunks);
+//       2. selection of the persistent units (whole units of up to 32K tokens in a large
+//          launch, else chunks);
 //       3. attention splits of the reused units, then of the persistent units, then of
 //          the missed units.
 //     A selection scores every cached token, score[t] = sum_g (128 - popc(qcode_g ^
@@ -84,10 +84,10 @@ struct AttSmem {
 };
 
 struct SelSmem {
-  uint16_t scores[kSelChunkMax];    // scores of the chunk's tokens
-  uint32_t hist[kCompWarps][kNBPad]; // histogram of each warp's segment of the chunk
-  uint32_t tot[kNBPad];             // the unit's histogram (last chunk to arrive)
-  int wc[kCompWarps][2];
+  uint16_t scores[kSelChunkMax];     // scores of the chunk's tokens
+  uint32_t hist[kCompWarps][kNBPad]; // each warp's histogram: counts of its two halves in 16-bit halves
+  uint32_t tot[kNBPad];              // the unit's histogram (last chunk to arrive)
+  int wc[kCompWarps][4];             // {above T, at T} of each warp's first and second half
   int misc[8];
 };
 
@@ -95,7 +95,8 @@ struct SelSmem {
 struct SelUnitSmem {
   uint16_t scores[32768];
   uint32_t hist[kNBPad];
-  int wc[kCompWarps][2];
+  int wc[kCompWarps][4];  // {above T, at T} of each warp's first and second half
+  int2 thr;               // {T, count above T}
   int misc[8];
 };
 
@@ -207,22 +208,121 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
 // ---- selection item: one chunk of sel_chunk tokens of one unit -------------------------
 // Scores are small integers (0 .. 128 G), so the top-k is one histogram digit:
 //   1. each warp scores its contiguous quarter of the chunk (16-byte codes read once,
-//      coalesced), keeps the scores in shared memory and builds its own histogram; the
-//      chunk's histogram is added into the unit's histogram in global memory;
+//      coalesced), keeps the scores in shared memory and counts them in its own histogram,
+//      the two halves of its quarter in the low and high 16 bits of each bin; the chunk's
+//      histogram is added into the unit's histogram in global memory;
 //   2. the chunk that arrives last finds the unit's threshold T, the largest score with
 //      count(score >= T) >= k, and publishes T and n_gt = count(score > T);
 //   3. each chunk publishes its counts above and at T; from the counts of the chunks
 //      before it, a chunk knows where its indices go and how many of its ties it takes
 //      (ties go to the lowest token index: the quota k - n_gt is filled in chunk order);
-//   4. ordered compaction of each warp's quarter from the scores in shared memory.
+//   4. ordered compaction: each warp writes the indices of its two half-quarters as two
+//      independent streams, 4 tokens per lane per round; a lane's output position comes
+//      from ballots of the counts above and at T, so only sums are carried from round to
+//      round.
 // The chunks of a unit sit next to each other in the work queue and every group runs its
 // item to the end, so the waits of steps 2 and 3 only target items already running
 // (provided at least nch groups run; the host checks this).
+
+// Largest score T with count(score >= T) >= k from a histogram tot[0..NB) in shared
+// memory, by all 128 threads of the group; writes {T, count(score > T)} to *res (only
+// the thread whose bins hold the crossing writes).
+template <int NB>
+__device__ __forceinline__ void find_threshold(const uint32_t* tot, int k, int2* res, int* red, int gtid) {
+  constexpr int SEG = (NB + kCompThreads - 1) / kCompThreads;  // bins per thread, from the top
+  const int warp = gtid >> 5, lane = gtid & 31;
+  const int hi = NB - gtid * SEG;
+  const int lo = hi - SEG > 0 ? hi - SEG : 0;
+  int segsum = 0;
+#pragma unroll
+  for (int i = 0; i < SEG; ++i)
+    if (hi - 1 - i >= lo) segsum += (int)tot[hi - 1 - i];
+  int incl = segsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) red[warp] = incl;
+  comp_bar();
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < kCompWarps; ++w) before += w < warp ? red[w] : 0;
+  incl += before;
+  const int excl = incl - segsum;  // count of scores above this thread's bins
+  if (excl < k && incl >= k) {
+    int run = excl;
+    for (int bin = hi - 1; bin >= lo; --bin) {
+      if (run + (int)tot[bin] >= k) {
+        *res = make_int2(bin, run);
+        break;
+      }
+      run += (int)tot[bin];
+    }
+  }
+}
+
+// Ordered compaction of one stream of a warp: tokens [a, b) of the chunk (a, b multiples
+// of 4; b - a a multiple of 128 except at the chunk's end), state {off, eqb}: the next
+// output position and the number of ties (score == T) before a in the chunk.
+struct CompactStream {
+  int a, b, off, eqb;
+};
+
+__device__ __forceinline__ void compact_round(const uint16_t* scores, CompactStream& st, int base, int T,
+                                              int take_eq, int64_t t0, int32_t* out, int k, uint32_t* err,
+                                              int lane) {
+  const uint32_t lt = (1u << lane) - 1u;
+  const int t = base + 4 * lane;
+  int sc[4];
+  if (t + 3 < st.b) {
+    const uint2 v = *reinterpret_cast<const uint2*>(&scores[t]);
+    sc[0] = (int)(v.x & 0xffffu);
+    sc[1] = (int)(v.x >> 16);
+    sc[2] = (int)(v.y & 0xffffu);
+    sc[3] = (int)(v.y >> 16);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sc[j] = t + j < st.b ? (int)scores[t + j] : -1;
+  }
+  int ngt = 0, neq = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    ngt += sc[j] > T;
+    neq += sc[j] == T;
+  }
+  const uint32_t g0 = __ballot_sync(0xffffffffu, ngt & 1), g1 = __ballot_sync(0xffffffffu, ngt & 2),
+                 g2 = __ballot_sync(0xffffffffu, ngt & 4);
+  const uint32_t e0 = __ballot_sync(0xffffffffu, neq & 1), e1 = __ballot_sync(0xffffffffu, neq & 2),
+                 e2 = __ballot_sync(0xffffffffu, neq & 4);
+  const int gt_lt = __popc(g0 & lt) + 2 * __popc(g1 & lt) + 4 * __popc(g2 & lt);
+  const int eq_lt = __popc(e0 & lt) + 2 * __popc(e1 & lt) + 4 * __popc(e2 & lt);
+  const int q = max(take_eq - st.eqb, 0);  // ties still to take at the start of the round
+  int e_run = eq_lt;                       // ties of the round before this lane's tokens
+  int pos = st.off + gt_lt + min(q, eq_lt);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool is_eq = sc[j] == T;
+    if (sc[j] > T || (is_eq && e_run < q)) {
+      if (pos < k)
+        out[pos] = (int32_t)(t0 + t + j);
+      else
+        atomicOr(err, kErrBounds);
+      ++pos;
+    }
+    e_run += is_eq;
+  }
+  const int round_eq = __popc(e0) + 2 * __popc(e1) + 4 * __popc(e2);
+  st.off += __popc(g0) + 2 * __popc(g1) + 4 * __popc(g2) + min(q, round_eq);
+  st.eqb += round_eq;
+}
+
 template <int G>
 __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int CH, int NC, int gtid) {
   constexpr int NB = 128 * G + 1;
   constexpr int kU = 8;                          // code loads in flight per lane
   const int WSEG = CH / kCompWarps;              // tokens per warp (CH: 1024 .. 16384), a multiple of 32 * kU
+  const int HSEG = WSEG / 2;                     // tokens per half-quarter, a multiple of 128
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
   const int k = s.kcount[b];
@@ -238,6 +338,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   // 1. scores and histograms of this warp's segment [w0, w1)
   const int w0 = warp * WSEG;
   const int w1 = (w0 + WSEG < len) ? w0 + WSEG : len;
+  const int wmid = w0 + HSEG;  // first token of the second half
   const uint4* src = s.codes + u * s.Nmax + t0;
   constexpr int kPfRounds = 4;  // L2 prefetch of the codes this many rounds ahead
   if (lane == 0)
@@ -262,7 +363,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
       if (t < w1) {
         const int sc = score_of<G>(cv[j], qp);
         sm.scores[t] = (uint16_t)sc;
-        atomicAdd(&wh[sc], 1u);
+        atomicAdd(&wh[sc], t < wmid ? 1u : 65536u);  // counts of a half fit 16 bits (<= 8192)
       }
     }
   }
@@ -271,7 +372,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   for (int i = gtid; i < NB; i += kCompThreads) {
     uint32_t v = 0;
 #pragma unroll
-    for (int w = 0; w < kCompWarps; ++w) v += sm.hist[w][i];
+    for (int w = 0; w < kCompWarps; ++w) v += (sm.hist[w][i] & 0xffffu) + (sm.hist[w][i] >> 16);
     if (v) atomicAdd(UH + i, v);
   }
   comp_bar();  // the group's additions happen before gtid 0's release below
@@ -281,38 +382,26 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   // 2. threshold (last chunk to arrive) or wait for it.  The last chunk also zeroes the
   //    unit's histogram for the next step (every chunk has added to it by now).
   if (sm.misc[0]) {
-    for (int i = gtid; i < NB; i += kCompThreads) {
-      sm.tot[i] = __ldcg(UH + i);
-      UH[i] = 0u;
+    constexpr int PER = (NB + kCompThreads - 1) / kCompThreads;
+    uint32_t v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int bin = gtid + i * kCompThreads;
+      v[i] = bin < NB ? __ldcg(UH + bin) : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int bin = gtid + i * kCompThreads;
+      if (bin < NB) {
+        sm.tot[bin] = v[i];
+        UH[bin] = 0u;
+      }
     }
     comp_bar();
-    if (warp == 0) {
-      const int seg = (NB + 31) / 32;
-      const int hi = NB - lane * seg;
-      const int lo = hi - seg > 0 ? hi - seg : 0;
-      int segsum = 0;
-      for (int bin = lo; bin < hi; ++bin) segsum += (int)sm.tot[bin];
-      int incl = segsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int excl = incl - segsum;
-      if (excl < k && incl >= k) {
-        int run = excl;
-        for (int bin = hi - 1; bin >= lo; --bin) {
-          if (run + (int)sm.tot[bin] >= k) {
-            s.sel_thr[u] = make_int2(bin, run);
-            break;
-          }
-          run += (int)sm.tot[bin];
-        }
-      }
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) red_release_add_u32(&s.fin_done[u], 1u);
-    }
+    find_threshold<NB>(sm.tot, k, &s.sel_thr[u], &sm.misc[4], gtid);
+    __threadfence();
+    comp_bar();  // the crossing thread's write happens before gtid 0's release
+    if (gtid == 0) red_release_add_u32(&s.fin_done[u], 1u);
   }
   if (gtid == 0) {
     wait_flag(&s.fin_done[u], 1u, s, 256);
@@ -324,26 +413,34 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   const int T = sm.misc[1], n_gt = sm.misc[2];
   const int quota = k - n_gt;  // ties to take, unit-wide, lowest index first
 
-  // 3. counts of each warp's segment; the chunk's counts; offsets from earlier chunks
+  // 3. counts of each half-quarter: {above T, at T} of the first and second half
   {
-    int gt = 0;
-    for (int bin = T + 1 + lane; bin < NB; bin += 32) gt += (int)wh[bin];
+    int gl = 0, gh = 0;
+    for (int bin = T + 1 + lane; bin < NB; bin += 32) {
+      gl += (int)(wh[bin] & 0xffffu);
+      gh += (int)(wh[bin] >> 16);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      gl += __shfl_xor_sync(0xffffffffu, gl, o);
+      gh += __shfl_xor_sync(0xffffffffu, gh, o);
+    }
     if (lane == 0) {
-      sm.wc[warp][0] = gt;
-      sm.wc[warp][1] = (int)wh[T];
+      sm.wc[warp][0] = gl;
+      sm.wc[warp][1] = (int)(wh[T] & 0xffffu);
+      sm.wc[warp][2] = gh;
+      sm.wc[warp][3] = (int)(wh[T] >> 16);
     }
   }
   comp_bar();
   int eq_c = 0;
 #pragma unroll
-  for (int w = 0; w < kCompWarps; ++w) eq_c += sm.wc[w][1];
+  for (int w = 0; w < kCompWarps; ++w) eq_c += sm.wc[w][1] + sm.wc[w][3];
   if (warp == 0) {
     if (lane == 0) {
       int gt_c = 0;
 #pragma unroll
-      for (int w = 0; w < kCompWarps; ++w) gt_c += sm.wc[w][0];
+      for (int w = 0; w < kCompWarps; ++w) gt_c += sm.wc[w][0] + sm.wc[w][2];
       s.sel_meta[u * NC + c] = make_int2(gt_c, eq_c);
       __threadfence();
       red_release_add_u32(&s.cnt_done[u], 1u);
@@ -376,42 +473,70 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   int take_eq = quota - sm.misc[4];  // ties this chunk takes
   take_eq = take_eq < 0 ? 0 : (take_eq > eq_c ? eq_c : take_eq);
 
-  // 4. ordered compaction of this warp's segment
-  int off = sm.misc[3], eqb = 0;
-  for (int w = 0; w < warp; ++w) {
-    int tk = take_eq - eqb;
-    tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);
-    off += sm.wc[w][0] + tk;
-    eqb += sm.wc[w][1];
-  }
+  // 4. ordered compaction of the warp's two half-quarters as independent streams
+  CompactStream sa, sb;
   {
-    const uint32_t lt = (1u << lane) - 1u;
-    int32_t* out = s.idx + u * s.kmax;
-    for (int base = w0; base < w1; base += 32) {
-      const int t = base + lane;
-      const int sc = t < w1 ? (int)sm.scores[t] : -1;
-      const bool is_eq = sc == T;
-      const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-      const bool sel = sc > T || (is_eq && eqb + __popc(beq & lt) < take_eq);
-      const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
-      if (sel) {
-        const int pos = off + __popc(bsel & lt);
-        if (pos < k)
-          out[pos] = (int32_t)(t0 + t);
-        else
-          atomicOr(s.err, kErrBounds);
+    int off = sm.misc[3], eqb = 0;
+    for (int w = 0; w <= warp; ++w)
+      for (int hf = 0; hf < 2; ++hf) {
+        if (w == warp && hf == 0) {
+          sa.off = off;
+          sa.eqb = eqb;
+        } else if (w == warp) {
+          sb.off = off;
+          sb.eqb = eqb;
+          break;
+        }
+        const int g = sm.wc[w][2 * hf], e = sm.wc[w][2 * hf + 1];
+        off += g + min(max(take_eq - eqb, 0), e);
+        eqb += e;
       }
-      eqb += __popc(beq);
-      off += __popc(bsel);
-    }
+  }
+  sa.a = w0;
+  sa.b = wmid < w1 ? wmid : w1;
+  sb.a = wmid;
+  sb.b = w1;
+  int32_t* out = s.idx + u * s.kmax;
+  for (int r = 0; r < HSEG; r += 128) {
+    if (sa.a + r < sa.b) compact_round(sm.scores, sa, sa.a + r, T, take_eq, t0, out, k, s.err, lane);
+    if (sb.a + r < sb.b) compact_round(sm.scores, sb, sb.a + r, T, take_eq, t0, out, k, s.err, lane);
   }
   comp_bar();  // the group's index writes happen before gtid 0's release
   if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
 }
 
+// Counts of scores above and at T in tokens [a, b) of shared memory, summed over the warp
+// (4 tokens per lane per round; a a multiple of 4).
+__device__ __forceinline__ int2 count_stream(const uint16_t* scores, int a, int b, int T, int lane) {
+  int gt = 0, eq = 0;
+  for (int base = a; base < b; base += 128) {
+    const int t = base + 4 * lane;
+    if (t + 3 < b) {
+      const uint2 v = *reinterpret_cast<const uint2*>(&scores[t]);
+      const int s0 = (int)(v.x & 0xffffu), s1 = (int)(v.x >> 16), s2 = (int)(v.y & 0xffffu), s3 = (int)(v.y >> 16);
+      gt += (s0 > T) + (s1 > T) + (s2 > T) + (s3 > T);
+      eq += (s0 == T) + (s1 == T) + (s2 == T) + (s3 == T);
+    } else {
+      for (int j = 0; j < 4; ++j)
+        if (t + j < b) {
+          const int sc = (int)scores[t + j];
+          gt += sc > T;
+          eq += sc == T;
+        }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+  }
+  return make_int2(gt, eq);
+}
+
 // ---- selection item: a whole unit (contexts up to 32K tokens) ----------------------------
 // One compute group scores all of the unit's tokens into shared memory, finds the
-// threshold T from its histogram and compacts: no hand-off with other groups.
+// threshold T from its histogram, counts each warp's half-quarters and compacts them as
+// in a chunk: no hand-off with other groups.
 template <int G>
 __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid) {
   constexpr int NB = 128 * G + 1;
@@ -421,6 +546,7 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
   const int k = s.kcount[b];
   const int warp = gtid >> 5, lane = gtid & 31;
   const int WSEG = (((N + kCompWarps - 1) / kCompWarps) + 255) / 256 * 256;  // tokens per warp
+  const int HSEG = WSEG / 2;
   for (int i = gtid; i < NB; i += kCompThreads) sm.hist[i] = 0;
   QPlanes<G> qp;
   load_qplanes<G>(s, u, qp);
@@ -456,79 +582,48 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
     }
   }
   comp_bar();
-  if (warp == 0) {  // threshold T: largest score with count(score >= T) >= k
-    const int seg = (NB + 31) / 32;
-    const int hi = NB - lane * seg;
-    const int lo = hi - seg > 0 ? hi - seg : 0;
-    int segsum = 0;
-    for (int bin = lo; bin < hi; ++bin) segsum += (int)sm.hist[bin];
-    int incl = segsum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+  find_threshold<NB>(sm.hist, k, &sm.thr, &sm.misc[4], gtid);
+  comp_bar();
+  const int T = sm.thr.x < 0 ? 0 : (sm.thr.x >= NB ? NB - 1 : sm.thr.x);
+  const int take_eq = k - sm.thr.y;  // ties taken, lowest index first
+  const int wmid = w0 + HSEG;
+  CompactStream sa, sb;
+  sa.a = w0;
+  sa.b = wmid < w1 ? wmid : w1;
+  sb.a = wmid;
+  sb.b = w1;
+  {
+    const int2 ca = count_stream(sm.scores, sa.a, sa.b, T, lane);
+    const int2 cb = count_stream(sm.scores, sb.a, sb.b, T, lane);
+    if (lane == 0) {
+      sm.wc[warp][0] = ca.x;
+      sm.wc[warp][1] = ca.y;
+      sm.wc[warp][2] = cb.x;
+      sm.wc[warp][3] = cb.y;
     }
-    const int excl = incl - segsum;
-    if (excl < k && incl >= k) {
-      int run = excl;
-      for (int bin = hi - 1; bin >= lo; --bin) {
-        if (run + (int)sm.hist[bin] >= k) {
-          sm.misc[0] = bin;
-          sm.misc[1] = run;
+  }
+  comp_bar();
+  {
+    int off = 0, eqb = 0;
+    for (int w = 0; w <= warp; ++w)
+      for (int hf = 0; hf < 2; ++hf) {
+        if (w == warp && hf == 0) {
+          sa.off = off;
+          sa.eqb = eqb;
+        } else if (w == warp) {
+          sb.off = off;
+          sb.eqb = eqb;
           break;
         }
-        run += (int)sm.hist[bin];
+        const int g = sm.wc[w][2 * hf], e = sm.wc[w][2 * hf + 1];
+        off += g + min(max(take_eq - eqb, 0), e);
+        eqb += e;
       }
-    }
   }
-  comp_bar();
-  const int T = sm.misc[0];
-  const int take_eq = k - sm.misc[1];  // ties taken, lowest index first
-  {
-    int gt = 0, eq = 0;
-    for (int t = w0 + lane; t < w1; t += 32) {
-      const int sc = sm.scores[t];
-      gt += sc > T;
-      eq += sc == T;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o);
-      eq += __shfl_xor_sync(0xffffffffu, eq, o);
-    }
-    if (lane == 0) {
-      sm.wc[warp][0] = gt;
-      sm.wc[warp][1] = eq;
-    }
-  }
-  comp_bar();
-  int off = 0, eqb = 0;
-  for (int w = 0; w < warp; ++w) {
-    int tk = take_eq - eqb;
-    tk = tk < 0 ? 0 : (tk > sm.wc[w][1] ? sm.wc[w][1] : tk);
-    off += sm.wc[w][0] + tk;
-    eqb += sm.wc[w][1];
-  }
-  {
-    const uint32_t lt = (1u << lane) - 1u;
-    int32_t* out = s.idx + u * s.kmax;
-    for (int base = w0; base < w1; base += 32) {
-      const int t = base + lane;
-      const int sc = t < w1 ? (int)sm.scores[t] : -1;
-      const bool is_eq = sc == T;
-      const uint32_t beq = __ballot_sync(0xffffffffu, is_eq);
-      const bool sel = sc > T || (is_eq && eqb + __popc(beq & lt) < take_eq);
-      const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
-      if (sel) {
-        const int pos = off + __popc(bsel & lt);
-        if (pos < k)
-          out[pos] = t;
-        else
-          atomicOr(s.err, kErrBounds);
-      }
-      eqb += __popc(beq);
-      off += __popc(bsel);
-    }
+  int32_t* out = s.idx + u * s.kmax;
+  for (int r = 0; r < HSEG; r += 128) {
+    if (sa.a + r < sa.b) compact_round(sm.scores, sa, sa.a + r, T, take_eq, 0, out, k, s.err, lane);
+    if (sb.a + r < sb.b) compact_round(sm.scores, sb, sb.a + r, T, take_eq, 0, out, k, s.err, lane);
   }
   comp_bar();  // the group's index writes happen before gtid 0's release
   if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
@@ -1066,8 +1161,8 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     const int32_t* lst = list == 2 ? s.miss_list : (list == 1 ? s.pers_list : s.hit_list);
     if (s.timeline && gtid == 0) s_t0 = global_timer_ns();
     if (sec <= 1) {  // selection chunk
-      // missed units: chunks that select a unit soon (its fetch waits); persistent units:
-      // whole units when they fit one group (fewer, cheaper items), else chunks
+      // missed units' chunks first (their fetch waits for them), then persistent units':
+      // whole units when they fit one group's shared memory in a large launch, else chunks
       const int nc = sec == 0 ? s.nch_miss : NC;
       const int p = (int)(j / nc), c = (int)(j % nc);
       const int l = layer_of(pl, L, p);

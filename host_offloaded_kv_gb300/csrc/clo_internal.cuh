@@ -87,7 +87,7 @@ struct DevState {
   uint32_t* fin_done;           // [U] threshold published (zeroed per step)
   uint32_t* cnt_done;           // [U] chunk counts published (zeroed per step)
   uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
-  int sel_chunk;                // tokens per selection chunk of a persistent unit (Nmax: whole unit)
+  int sel_chunk;                // tokens per selection chunk of a persistent unit
   int nch;                      // selection chunks per persistent unit = ceil(Nmax / sel_chunk)
   int sel_chunk_miss;           // tokens per selection chunk of a missed unit
   int nch_miss;                 // selection chunks per missed unit
