@@ -399,6 +399,7 @@ def run_gb300(args, rank, world, local_rank):
     ms_total = ev0.elapsed_time(ev1)
     st = lib.stats()
     timeline = lib.timeline()
+    step_bytes = lib.step_bytes(n_prof + W, n_prof + W + K)   # [K][2] host, HBM bytes of each timed step
     if timeline is not None:
         timeline["host_bytes"] = st["last_host_bytes"]
     host_bytes = st["host_bytes"] - before["host_bytes"]
@@ -463,7 +464,13 @@ def run_gb300(args, rank, world, local_rank):
                 "hbm_bytes_per_launch": hbm_bytes / steps, "host_bytes_per_launch": host_bytes / steps,
                 "peak_source": {"hbm": f"MEASURED_PEAKS.json hbm_gbs ({hbm_src})",
                                 "host-link": "pinned H2D copy, best of 16 timed 1 GiB copies in this run"}}
-    step_ideal_ms = max(hbm_bytes / (hbm_peak * 1e9), host_bytes / (link_gbs * 1e9)) * 1e3 / steps
+    # steps run one after another, so the roofline of the run is the sum over its steps of
+    # each step's max(HBM bytes / HBM peak, host bytes / link peak); the max of the
+    # run's averaged bytes (aggregate form) understates it when link-bound and HBM-bound
+    # steps alternate
+    per_step = [max(m / (hbm_peak * 1e9), h / (link_gbs * 1e9)) for h, m in step_bytes.tolist()]
+    step_ideal_ms = sum(per_step) * 1e3 / steps
+    aggregate_ideal_ms = max(hbm_bytes / (hbm_peak * 1e9), host_bytes / (link_gbs * 1e9)) * 1e3 / steps
     step_ms = ms_total / steps
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": W,
@@ -485,8 +492,11 @@ def run_gb300(args, rank, world, local_rank):
                       if args.grow else "")},
         "gpu_launches": steps * (2 * (L if args.layerwise else 1) + (3 if args.grow else 0)),
         "roofline": roofline,
-        "step_roofline": {"bound": "max(HBM alg bytes / HBM peak, host bytes / link peak)",
+        "step_roofline": {"bound": "sum over the timed steps of max(HBM alg bytes / HBM peak, host bytes / link peak)",
                           "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,
+                          "aggregate_ideal_ms": aggregate_ideal_ms, "aggregate_frac": aggregate_ideal_ms / step_ms,
+                          "link_bound_steps": sum(1 for h, m in step_bytes.tolist()
+                                                  if h / (link_gbs * 1e9) >= m / (hbm_peak * 1e9)),
                           "hbm_bytes_per_step": hbm_bytes / steps, "host_bytes_per_step": host_bytes / steps,
                           "link_peak_gbs": link_gbs, "hbm_peak_gbs": hbm_peak},
         "kernels": kern,

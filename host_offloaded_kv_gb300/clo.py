@@ -18,7 +18,9 @@ CLO_OK, CLO_ERR_INVALID, CLO_ERR_OOM, CLO_ERR_CUDA, CLO_ERR_TIMEOUT, CLO_ERR_STA
     CLO_ERR_DEVICE = range(8)
 CLO_DEC_HIT, CLO_DEC_MISS, CLO_DEC_PERSIST = 0, 1, 2
 (CLO_DBG_KEY_CODES, CLO_DBG_QUERY_CODES, CLO_DBG_IDX, CLO_DBG_DECISION, CLO_DBG_SLOT_ROWS, CLO_DBG_TAU,
- CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS, CLO_DBG_TIMELINE, CLO_DBG_TOPK, CLO_DBG_POOL_NODE) = range(1, 13)
+ CLO_DBG_PERSIST, CLO_DBG_SHAT, CLO_DBG_COS, CLO_DBG_TIMELINE, CLO_DBG_TOPK, CLO_DBG_POOL_NODE,
+ CLO_DBG_STEP_BYTES) = range(1, 14)
+STEP_HIST = 4096
 CLO_SET_DROP_FLAG_LAYER, CLO_SET_WAIT_TIMEOUT_NS = 1, 2
 
 _STATUS_NAMES = {0: "CLO_OK", 1: "CLO_ERR_INVALID", 2: "CLO_ERR_OOM", 3: "CLO_ERR_CUDA", 4: "CLO_ERR_TIMEOUT",
@@ -284,6 +286,15 @@ class CLOContext:
             self.close()
         except Exception:
             pass
+
+    def step_bytes(self, first: int, last: int) -> np.ndarray:
+        """Host-link and algorithmic HBM bytes of each step in [first, last) (timing mode):
+        int64 [last - first][2], from the library's cumulative per-step history."""
+        if last - first + 1 > STEP_HIST or first < 1:
+            raise ValueError("the history keeps the last 4096 steps and needs the step before the first")
+        h = clo_debug_get(self.ctx, CLO_DBG_STEP_BYTES, 0, 0, 0, np.empty((STEP_HIST, 2), dtype=np.uint64))
+        cum = np.array([h[s % STEP_HIST] for s in range(first - 1, last)], dtype=np.int64)
+        return np.diff(cum, axis=0)
 
     def pool_node(self) -> int:
         """NUMA node of the pinned pool's pages, or -1 when the pool was not placed."""

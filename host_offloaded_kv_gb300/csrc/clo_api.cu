@@ -310,7 +310,10 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   s.rec_bytes = (int)rec;
   s.wait_timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : 2000000000LL;
   s.drop_flag_layer = cfg->debug_drop_flag_layer;
-  s.nsplit = (int)((c->kmax + kSplitRows - 1) / kSplitRows);
+  // long selections take 2048-row attention splits (fewer partials to merge, measured
+  // ~5 % faster on 512K contexts), short ones 1024 (more splits to spread the units)
+  s.split_rows = c->kmax > 8192 ? 2048 : 1024;
+  s.nsplit = (int)((c->kmax + s.split_rows - 1) / s.split_rows);
   s.nchunk = (int)((c->kmax + kChunkRows - 1) / kChunkRows);
   s.fetch_rows = kChunkRows;
   const int64_t U = c->U;
@@ -385,6 +388,11 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.sel_cnt = z + o_sel + 3 * U;
     c->timeline_dev = reinterpret_cast<unsigned long long*>(z + o_tl);
     s.timeline = cfg->timing ? c->timeline_dev : nullptr;
+  }
+  if (cfg->timing) {
+    CLO_TRY(c->dalloc(&s.step_bytes, (size_t)kStepHist * 2));
+  } else {
+    s.step_bytes = nullptr;
   }
   CLO_TRY(c->dalloc(&s.hit_list, (size_t)c->L * c->B * c->Hkv));
   CLO_TRY(c->dalloc(&s.pers_list, (size_t)c->L * c->B * c->Hkv));
@@ -594,6 +602,7 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   s.fetch_rows = frows;
   const bool warm = c->warmup_mode && c->step < c->W;
   s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
+  s.step_index = c->step;
   const bool timed = c->cfg.timing != 0;
   cudaEvent_t* ev = nullptr;
   if (timed) {
@@ -782,6 +791,11 @@ CLO_API clo_status clo_debug_get(clo_ctx* c, int32_t what, int32_t layer, int32_
     case CLO_DBG_TIMELINE:
       src = c->timeline_dev;
       bytes = (int64_t)kTimelineSlots * 8;
+      break;
+    case CLO_DBG_STEP_BYTES:
+      if (!s.step_bytes) return fail(CLO_ERR_STATE, "the per-step byte history needs timing mode");
+      src = s.step_bytes;
+      bytes = (int64_t)kStepHist * 16;
       break;
     case CLO_DBG_POOL_NODE: {  // host-side value
       if (dst_bytes < 4) return fail(CLO_ERR_INVALID, "dst too small: need 4 bytes");

@@ -631,7 +631,8 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
 
 // ---- attention split -----------------------------------------------------------------
 // Tensor-core (mma.sync m16n8k16, bf16 in, fp32 accumulate) split attention.  A split
-// is kSplitRows = 1024 selected rows; each of the 4 warps takes 256 of them in chunks of
+// is split_rows (1024, or 2048 for k > 8192) selected rows; each of the 4 warps takes a
+// quarter of them in chunks of
 // 16 rows fed through its own 2-stage ring in shared memory: every row of a chunk is one
 // 512-byte (d = 128) bulk copy on the TMA engine, issued by one lane and counted on the
 // stage's mbarrier, so the next chunk's rows land while this chunk's math runs.  Per
@@ -765,7 +766,7 @@ __device__ void attend_split(const DevState& s, AttSmem<D>& sm, uint64_t* bars, 
                              const uint16_t* __restrict__ q, float* __restrict__ out, int64_t u, int split,
                              int gtid) {
   constexpr int ROWW = AttSmem<D>::ROWW;
-  constexpr int WROWS = kSplitRows / kCompWarps;
+  const int WROWS = s.split_rows / kCompWarps;
   constexpr int ST = kAttStages;
   const int h = (int)(u % s.Hkv);
   const int b = (int)((u / s.Hkv) % s.B);
@@ -774,7 +775,7 @@ __device__ void attend_split(const DevState& s, AttSmem<D>& sm, uint64_t* bars, 
   const int warp = gtid >> 5, lane = gtid & 31, gid = lane >> 2, tig = lane & 3;
   const int64_t N = s.ntok[b];
   const int64_t k = s.kcount[b];
-  const int64_t r0 = (int64_t)split * kSplitRows + (int64_t)warp * WROWS;
+  const int64_t r0 = (int64_t)split * s.split_rows + (int64_t)warp * WROWS;
   const int64_t r1 = (r0 + WROWS < k) ? r0 + WROWS : k;
   const int nch = r1 > r0 ? (int)((r1 - r0 + 15) / 16) : 0;
   const bool persistent = s.decision[u] == CLO_DEC_PERSIST;
@@ -1121,6 +1122,18 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
     sec_start[0] = 0;
     for (int i = 0; i < 5; ++i) sec_start[i + 1] = sec_start[i] + size[i];
   }
+  if (s.step_bytes && s.l1 == s.L && blockIdx.x == 0 && tid == 0) {
+    // the step's last launch: its reuse decisions (and every earlier layer's) are counted,
+    // so the cumulative byte counters are the totals after this step
+    unsigned long long hb = 0, mb = 0;
+    for (int i = 0; i < kCtrLanes; ++i) {
+      hb += s.total_ctr[C_HOST_BYTES * kCtrLanes + i];
+      mb += s.total_ctr[C_HBM_BYTES * kCtrLanes + i];
+    }
+    const int64_t slot = (s.step_index % kStepHist) * 2;
+    s.step_bytes[slot] = hb;
+    s.step_bytes[slot + 1] = mb;
+  }
   if (s.adapt_active && blockIdx.x == 0) {
     // online thresholds: fold this step's mean adjacent-step cosine of each (layer,
     // kv head) into s_hat; the decide kernel, finished before this launch, summed them
@@ -1182,14 +1195,14 @@ __global__ void __launch_bounds__(32 * (FW + kCompWarps), MINB)
       const int l = layer_of(pl, L, p);
       const int64_t u = lst[(int64_t)l * BH + (p - pl[l])];
       const int b = (int)((u / s.Hkv) % s.B);
-      const int64_t r0 = (int64_t)c * kSplitRows;
+      const int64_t r0 = (int64_t)c * s.split_rows;
       if (s.timeline && gtid == 0) atomicCAS(&s.timeline[TL_ATT_FIRST], 0ull, s_t0);
       if (sec == 3) {
         if (gtid == 0) wait_flag(&s.sel_cnt[u], (uint32_t)NC, s);
         comp_bar();
       } else if (sec == 4 && r0 < s.kcount[b]) {
         if (gtid == 0) {
-          constexpr int kPer = kSplitRows / kChunkRows;  // the fetch chunks this split reads
+          const int kPer = s.split_rows / kChunkRows;  // the fetch chunks this split reads
           const uint32_t subs = (uint32_t)(kChunkRows / s.fetch_rows);  // fetch items per chunk
           for (int fc = c * kPer; fc < (c + 1) * kPer && (int64_t)fc * kChunkRows < s.kcount[b]; ++fc)
             wait_flag(&s.ready[u * s.nchunk + fc], subs, s);

@@ -71,7 +71,8 @@ struct DevState {
   uint32_t* err;                // error word
   uint32_t* unit_done;          // [U] split counters of the attention combine
   float* part;                  // attention partials [U][nsplit][G][d + 2] (one per split)
-  int nsplit;                   // attention splits per unit (kSplitRows rows each)
+  int nsplit;                   // attention splits per unit (split_rows rows each)
+  int split_rows;               // selected rows per attention split: 1024, or 2048 when kmax > 8192
   int nchunk;                   // fetch chunks per unit (kChunkRows rows each)
   int fetch_rows;               // rows per fetch item: 256, 128, 64 or 32 (divides kChunkRows)
   uint32_t* ready;              // [U][nchunk] fetch-ready flag per row chunk (zeroed per step)
@@ -104,11 +105,14 @@ struct DevState {
   float tau_offset;             // tau = s_hat - tau_offset
   int kv_bits;                  // host pool storage: 16 (bf16), 4 or 2
   int rec_bytes;                // bytes of one token's K|V record in the host pool
+  unsigned long long* step_bytes; // [kStepHist][2] cumulative {host, HBM} bytes after each step (timing mode), or null
+  int64_t step_index;           // the step this launch belongs to
   int l0, l1;                   // layers of this launch: [l0, l1)
   int q_l0;                     // layer of the first [B][Hq][d] block of the q / out buffers
 };
 
 constexpr int kMaxLayers = 256;
+constexpr int kStepHist = 4096;  // steps kept by the per-step byte history (a ring)
 
 // timeline slots of the fused step kernel (ns of %globaltimer; first = first writer)
 enum Timeline : int {
@@ -132,7 +136,6 @@ enum Timeline : int {
 };
 constexpr int kSelChunkMax = 16384;  // tokens per selection chunk, at most
 constexpr int kSelChunkMin = 1024;   // tokens per selection chunk, at least
-constexpr int kSplitRows = 1024;  // selected rows per attention split
 constexpr int kChunkRows = 256;   // selected rows per fetch chunk (one ready flag each)
 constexpr int kNBPad = 1056;     // >= 128 * kMaxG + 1, multiple of 32
 

@@ -245,10 +245,15 @@ CLO_API const char* clo_last_error(void);
  *                       [15] summed durations of attention splits after their waits
  *   CLO_DBG_TOPK        int32 [L][B]  top-k count k of each (layer, sequence) at its
  *                       current length (the rule of clo_config.topk / topk_ratio)
+ *   CLO_DBG_STEP_BYTES  uint64 [4096][2] timing mode only: cumulative {host-link bytes,
+ *                       algorithmic HBM bytes} since init after step s, at row s % 4096
+ *                       (written by the step's last launch; per-step bytes are the
+ *                       differences of consecutive rows)
  *   CLO_DBG_POOL_NODE   int32 [1]     NUMA node the pinned pool's pages were placed on
  *                       (-1: not placed: a host with one memory node, or placement failed
  *                       and the pool came from cudaHostAlloc)
- * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_CUDA. */
+ * Errors: CLO_ERR_INVALID (item, unit or size), CLO_ERR_STATE (CLO_DBG_STEP_BYTES without
+ * timing mode), CLO_ERR_CUDA. */
 enum {
   CLO_DBG_KEY_CODES = 1,
   CLO_DBG_QUERY_CODES = 2,
@@ -261,7 +266,8 @@ enum {
   CLO_DBG_COS = 9,
   CLO_DBG_TIMELINE = 10,
   CLO_DBG_TOPK = 11,
-  CLO_DBG_POOL_NODE = 12
+  CLO_DBG_POOL_NODE = 12,
+  CLO_DBG_STEP_BYTES = 13
 };
 CLO_API clo_status clo_debug_get(clo_ctx* ctx, int32_t what, int32_t layer, int32_t seq, int32_t kvh, void* dst,
                                  int64_t dst_bytes);
