@@ -310,9 +310,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   s.rec_bytes = (int)rec;
   s.wait_timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : 2000000000LL;
   s.drop_flag_layer = cfg->debug_drop_flag_layer;
-  // long selections take 2048-row attention splits (fewer partials to merge, measured
-  // ~5 % faster on 512K contexts), short ones 1024 (more splits to spread the units)
-  s.split_rows = c->kmax > 8192 ? 2048 : 1024;
+  // attention partials for the smallest split (256 rows, see enqueue_layers)
+  s.split_rows = 256;
   s.nsplit = (int)((c->kmax + s.split_rows - 1) / s.split_rows);
   s.nchunk = (int)((c->kmax + kChunkRows - 1) / kChunkRows);
   s.fetch_rows = kChunkRows;
@@ -600,6 +599,14 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   int frows = kChunkRows;
   while (frows > 32 && units * c->kmax / frows < 6LL * c->sms) frows /= 2;
   s.fetch_rows = frows;
+  // attention splits: long selections take 2048 rows (fewer partials to merge, measured
+  // ~5 % faster on 512K contexts), others 1024; a small launch takes 256 (one fetch chunk),
+  // so the attention that waits for the last fetched rows is short
+  const bool small = units < c->whole_unit_min_units;
+  s.split_rows = small ? 256 : (c->kmax > 8192 ? 2048 : 1024);
+  s.nsplit = (int)((c->kmax + s.split_rows - 1) / s.split_rows);
+  // query rows hashed per decide CTA: fewer in a small launch, for more CTAs
+  s.decide_rows = small ? 16 : 32;
   const bool warm = c->warmup_mode && c->step < c->W;
   s.adapt_active = (c->cfg.adaptive_tau && !warm) ? 1 : 0;
   s.step_index = c->step;

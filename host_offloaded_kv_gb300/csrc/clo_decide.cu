@@ -31,10 +31,10 @@ struct StridedBF16 {
   __device__ float operator()(int i) const { return bf16_bits_to_f32(p[i * stride]); }
 };
 
-// Units of one kv head handled by one CTA: as many sequences as fit 32 query rows,
+// Units of one kv head handled by one CTA: as many sequences as fit `rows` (<= 32) query rows,
 // at most one per warp.
-__host__ __device__ inline int units_per_cta(int G, int B) {
-  int n = kMaxRows / G;
+__host__ __device__ inline int units_per_cta(int G, int B, int rows) {
+  int n = (rows < kMaxRows ? rows : kMaxRows) / G;
   n = n < 1 ? 1 : (n > kDecideThreads / 32 ? kDecideThreads / 32 : n);
   return n < B ? n : B;
 }
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = s.G, d = s.d, GD = s.G * s.d;
-  const int UPC = units_per_cta(G, s.B);
+  const int UPC = units_per_cta(G, s.B, s.decide_rows);
   const int ngrp = (s.B + UPC - 1) / UPC;
   const int lh = s.l0 * s.Hkv + (int)(blockIdx.x / ngrp);
   const int b0 = (blockIdx.x % ngrp) * UPC;
@@ -279,7 +279,7 @@ __global__ void k_finish_warmup(DevState s, int W, float tau_offset, int n_persi
 
 template <int M>
 cudaError_t launch_decide_m(const DevState& s, const uint16_t* q, int64_t step, int warmup_active, cudaStream_t st) {
-  const int upc = units_per_cta(s.G, s.B);
+  const int upc = units_per_cta(s.G, s.B, s.decide_rows);
   const unsigned grid = (unsigned)((s.l1 - s.l0) * s.Hkv * ((s.B + upc - 1) / upc));
   const size_t smem = (size_t)s.d * 128 * 2 + (size_t)s.d * kHashSlots * M * 4;
   cudaError_t e = cudaFuncSetAttribute(k_decide<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -291,7 +291,7 @@ cudaError_t launch_decide_m(const DevState& s, const uint16_t* q, int64_t step, 
 cudaError_t launch_decide(const DevState& s, const uint16_t* q, int64_t step, int warmup_active,
                           cudaStream_t st) {
   // query rows per thread slot: enough for all rows of one CTA (at most 32 rows)
-  const int rows = units_per_cta(s.G, s.B) * s.G;
+  const int rows = units_per_cta(s.G, s.B, s.decide_rows) * s.G;
   const int per_slot = (rows + kHashSlots - 1) / kHashSlots;
   if (per_slot <= 4) return launch_decide_m<4>(s, q, step, warmup_active, st);
   return launch_decide_m<8>(s, q, step, warmup_active, st);

@@ -72,7 +72,8 @@ struct DevState {
   uint32_t* unit_done;          // [U] split counters of the attention combine
   float* part;                  // attention partials [U][nsplit][G][d + 2] (one per split)
   int nsplit;                   // attention splits per unit (split_rows rows each)
-  int split_rows;               // selected rows per attention split: 1024, or 2048 when kmax > 8192
+  int split_rows;               // selected rows per attention split: 256 (small launches), 1024, 2048 (kmax > 8192)
+  int decide_rows;              // query rows hashed per decide CTA: 32, or 16 in small launches
   int nchunk;                   // fetch chunks per unit (kChunkRows rows each)
   int fetch_rows;               // rows per fetch item: 256, 128, 64 or 32 (divides kChunkRows)
   uint32_t* ready;              // [U][nchunk] fetch-ready flag per row chunk (zeroed per step)
