@@ -249,7 +249,7 @@ def rank_plan(args, rank, world, local_rank):
     """What one replica runs: its device, its own seed (independent sequences per rank)
     and the bytes of its pinned host pool."""
     w = workload_from_args(args)
-    rec_bytes = 4 * w.head_dim if args.kv_bits == 16 else 2 * w.head_dim * args.kv_bits // 8 + (2 * w.head_dim // 64) * 8
+    rec_bytes = 4 * w.head_dim if args.kv_bits == 16 else 2 * w.head_dim * args.kv_bits // 8
     n_grow = ((w.warmup_steps if w.tau_fixed is None else 0) + args.warmup + 2 * args.steps + 1) if args.grow else 0
     ncap = w.n_tokens + n_grow
     pool = w.n_layers * w.batch * w.n_kv_heads * ncap * rec_bytes
@@ -303,7 +303,7 @@ def run_gb300(args, rank, world, local_rank):
 
     w = workload_from_args(args)
     L, B, Hq, Hkv, d, N = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_tokens
-    rec_bytes = 4 * d if args.kv_bits == 16 else 2 * d * args.kv_bits // 8 + (2 * d // 64) * 8
+    rec_bytes = 4 * d if args.kv_bits == 16 else 2 * d * args.kv_bits // 8
     K, W = args.steps, args.warmup
     n_grow = (w.warmup_steps if w.tau_fixed is None else 0) + W + 2 * K + 1 if args.grow else 0
     Ncap = N + n_grow                       # growth appends one token per step
@@ -481,7 +481,7 @@ def run_gb300(args, rank, world, local_rank):
                    "tau": (f"s_hat-{w.tau_offset} after {w.warmup_steps} profiling steps" if tau is None
                            else f"{w.tau_fixed} fixed") + (", then adaptive (running average, weight 1/16)"
                                                            if args.adaptive_tau else ""), "kv_dtype": "bf16" if args.kv_bits == 16 else
-                   f"int{args.kv_bits} host pool (asymmetric, 64-channel groups, fp32 scale/min), bf16 on the GPU", "parallelism": f"replicas x{world} (independent sequences)",
+                   f"int{args.kv_bits} host pool (asymmetric, 64-channel groups; fp32 scale/min in HBM), bf16 on the GPU", "parallelism": f"replicas x{world} (independent sequences)",
                    "l2": "inputs larger than L2 (host pool %.0f GiB, HBM codes+slots+resident per step > 1 GB)" %
                          (pool_bytes / 2**30),
                    "hit_rate_nonpersistent": hits / max(1, hits + miss),

@@ -272,8 +272,8 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   if (!can_map) return fail(CLO_ERR_CUDA, "device cannot map host memory");
 
   // pinned, device-mapped host pool: [U][Nmax][K|V record]
-  const size_t rec = c->kv_bits == 16 ? (size_t)4 * c->d
-                                      : (size_t)2 * c->d * c->kv_bits / 8 + (size_t)(2 * c->d / 64) * 8;
+  // a quantised record holds the codes only; the groups' (scale, min) pairs live in HBM
+  const size_t rec = c->kv_bits == 16 ? (size_t)4 * c->d : (size_t)2 * c->d * c->kv_bits / 8;
   const size_t pool_bytes = (size_t)c->U * (size_t)c->Nmax * rec;
   void* hp = nullptr;
   c->pool_bytes = pool_bytes;
@@ -340,6 +340,11 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
   CLO_TRY(c->dalloc(&s.cosv, (size_t)U));
   CLO_TRY(c->dalloc(&s.idx, (size_t)U * c->kmax));
   CLO_TRY(c->dalloc(&s.slots, (size_t)U * c->kmax * 2 * c->d));
+  if (c->kv_bits != 16) {
+    CLO_TRY(c->dalloc(&s.qparams, (size_t)U * c->Nmax * (2 * c->d / 64)));
+  } else {
+    s.qparams = nullptr;
+  }
   if (c->P > 0) {
     CLO_TRY(c->dalloc(&s.resident, (size_t)c->L * c->B * c->P * c->Nmax * 2 * c->d));
   } else {
@@ -582,12 +587,12 @@ static clo_status enqueue_layers(clo_ctx* c, int l0, int l1, const uint16_t* qd,
   s.q_l0 = l0;
   const int64_t units = (int64_t)(l1 - l0) * c->B * c->Hkv;
   // chunks of 8192 (contexts up to 32K) or 16384 tokens, halved (down to 1024) while the
-  // launch's units would give fewer than 4 chunks per SM: a launch with few units (one
+  // launch's units would give fewer than 8 chunks per SM: a launch with few units (one
   // layer, a small batch) spreads each selection over more compute groups.  All chunks
   // of a unit run at once (their waits need it), so a unit has at most one chunk per SM.
   int chunk = c->Nmax <= 32768 ? 8192 : kSelChunkMax;
   auto nchunks = [&](int ch) { return (c->Nmax + ch - 1) / ch; };
-  while (chunk > kSelChunkMin && units * nchunks(chunk) < 4LL * c->sms && nchunks(chunk / 2) <= c->sms) chunk /= 2;
+  while (chunk > kSelChunkMin && units * nchunks(chunk) < 8LL * c->sms && nchunks(chunk / 2) <= c->sms) chunk /= 2;
   s.sel_chunk_miss = chunk;
   // persistent units of contexts up to 32K are selected whole by one group (no waits on
   // other groups) when the launch holds units enough to occupy the groups

@@ -135,12 +135,11 @@ __global__ void k_pool_write(DevState s, int l, int b, int64_t t0, int64_t n, co
 // Quantises one 64-channel group (values at src, 16-byte aligned) into record rec:
 //   mn, mx of the group (a zero minimum as +0); scale = (mx - mn) / (2^BITS - 1);
 //   q = clamp(rint((x - mn) / scale), 0, 2^BITS - 1), 0 when scale is 0
-// (every operation fp32, rounded to nearest).  Codes and (scale, mn) go to the record;
-// resident (or null) gets the dequantised values.
+// (every operation fp32, rounded to nearest).  The codes go to the record, (scale, mn)
+// to the token's parameters in HBM; resident (or null) gets the dequantised values.
 template <int D, int BITS>
-__device__ __forceinline__ void quantise_group(const uint16_t* src, unsigned char* rec, int kv, int g,
+__device__ __forceinline__ void quantise_group(const uint16_t* src, unsigned char* rec, float2* params, int kv, int g,
                                                uint16_t* resident) {
-  using Q = QRec<D, BITS>;
   constexpr int NG = D / 64;  // groups per row
   constexpr float kLevels = (float)((1 << BITS) - 1);
   float x[64];
@@ -175,7 +174,7 @@ __device__ __forceinline__ void quantise_group(const uint16_t* src, unsigned cha
 #pragma unroll
   for (int v = 0; v < BITS / 2; ++v)
     codes[v] = make_uint4(words[4 * v], words[4 * v + 1], words[4 * v + 2], words[4 * v + 3]);
-  *reinterpret_cast<float2*>(rec + Q::kParamOff + 8 * (kv * NG + g)) = make_float2(scale, mn);
+  params[kv * NG + g] = make_float2(scale, mn);
   if (resident) {
     uint4* dst = reinterpret_cast<uint4*>(resident);
 #pragma unroll
@@ -204,7 +203,8 @@ __global__ void k_pool_write_q(DevState s, int l, int b, int64_t t0, int64_t n, 
     uint16_t* res = nullptr;
     if (p >= 0 && s.resident != nullptr)
       res = s.resident + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax + t0 + t) * 2 * D + kv * D + 64 * g;
-    quantise_group<D, BITS>(src, pool + (u * s.Nmax + t0 + t) * Q::kBytes, kv, g, res);
+    quantise_group<D, BITS>(src, pool + (u * s.Nmax + t0 + t) * Q::kBytes, s.qparams + (u * s.Nmax + t0 + t) * Q::kGroups,
+                            kv, g, res);
   }
 }
 
@@ -252,7 +252,8 @@ __global__ void k_step_pool_write_q(DevState s, const uint16_t* __restrict__ K, 
     uint16_t* res = nullptr;
     if (p >= 0 && s.resident != nullptr)
       res = s.resident + ((((int64_t)l * s.B + b) * s.P + p) * s.Nmax + t) * 2 * D + kv * D + 64 * g;
-    quantise_group<D, BITS>((kv == 0 ? K : V) + lbh * D + 64 * g, pool + (lbh * s.Nmax + t) * Q::kBytes, kv, g, res);
+    quantise_group<D, BITS>((kv == 0 ? K : V) + lbh * D + 64 * g, pool + (lbh * s.Nmax + t) * Q::kBytes,
+                            s.qparams + (lbh * s.Nmax + t) * Q::kGroups, kv, g, res);
   }
 }
 

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kDecideThreads) k_decide(DevState s, const uin
       int64_t hbm = (int64_t)GD * 2 + (int64_t)GD * 4 + (valid ? (int64_t)GD * 2 : 0) + k * rec;
       if (dec != CLO_DEC_HIT) hbm += N * 16 + k * 4;
       if (dec == CLO_DEC_MISS) hbm += (int64_t)GD * 2 + k * rec;
+      if (dec == CLO_DEC_MISS && s.kv_bits != 16) hbm += k * (2 * d / 64) * 8;  // groups' (scale, min)
       if (dec == CLO_DEC_PERSIST) hbm += k * 4;
       const int slot = dec == CLO_DEC_HIT ? C_HIT : (dec == CLO_DEC_MISS ? C_MISS : C_PERSIST);
       atomicAdd(&s.step_ctr[ctr_at(slot, u)], 1ull);

@@ -990,8 +990,9 @@ __device__ __forceinline__ void copy_rows(const DevState& s, int64_t u, int64_t 
   }
 }
 
-// Quantised records: lane (row slot, code vector j) loads one 16-byte code vector and
-// its group's (scale, min), and writes the dequantised bf16 values to the slot row.
+// Quantised records: lane (row slot, code vector j) loads one 16-byte code vector from the
+// host pool and its group's (scale, min) from HBM, and writes the dequantised bf16 values
+// to the slot row.
 template <int D, int FU, int BITS>
 __device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_t r0, int nr, const int32_t* sidx,
                                             int lane) {
@@ -999,6 +1000,7 @@ __device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_
   constexpr int PV = Q::kCodeVecs;  // lanes per row
   constexpr int RPI = 32 / PV;      // rows per warp-wide round
   const unsigned char* pool = reinterpret_cast<const unsigned char*>(s.pool) + u * s.Nmax * Q::kBytes;
+  const float2* params = s.qparams + u * s.Nmax * Q::kGroups;
   uint4* slot = reinterpret_cast<uint4*>(s.slots) + (u * s.kmax + r0) * (D / 4);
   const int rl = lane / PV, j = lane % PV, gi = j / Q::kVecsPerGroup;
   for (int rb = 0; rb < nr; rb += RPI * FU) {
@@ -1012,9 +1014,8 @@ __device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_
       if (r < nr) {
         const int t = sidx[r];
         if (t >= 0) {
-          const unsigned char* rec = pool + (int64_t)t * Q::kBytes;
-          cv[f] = ld_nc_v4(reinterpret_cast<const uint4*>(rec) + j);
-          pp[f] = ld_nc_f2(rec + Q::kParamOff + 8 * gi);
+          cv[f] = ld_nc_v4(reinterpret_cast<const uint4*>(pool + (int64_t)t * Q::kBytes) + j);
+          pp[f] = __ldg(params + (int64_t)t * Q::kGroups + gi);
         }
       }
     }
@@ -1026,10 +1027,6 @@ __device__ __forceinline__ void copy_rows_q(const DevState& s, int64_t u, int64_
   }
 }
 
-// A fetch item is fetch_rows (256, 128, 64 or 32) rows of one chunk of kChunkRows; every
-// item of a chunk (empty ones too) adds 1 to the chunk's ready flag, which is complete at
-// kChunkRows / fetch_rows.  Launches with few missed rows use small items, so the rows
-// of a layer are spread over many fetch warps.
 template <int D, int FU>
 __device__ void fetch_role(const DevState& s, const int* pre_m, int n_miss, int lane, int32_t* sidx) {
   constexpr int kFetchUnroll = FU;
@@ -1278,12 +1275,13 @@ template <int D, int BITS>
 __device__ __forceinline__ void fill_q(const DevState& s, int64_t u, int64_t t0, int64_t t1, uint4* dst) {
   using Q = QRec<D, BITS>;
   const unsigned char* pool = reinterpret_cast<const unsigned char*>(s.pool) + (u * s.Nmax + t0) * Q::kBytes;
+  const float2* params = s.qparams + (u * s.Nmax + t0) * Q::kGroups;
   const int64_t n = (t1 - t0) * Q::kCodeVecs;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = e / Q::kCodeVecs;
     const int j = (int)(e % Q::kCodeVecs);
     const unsigned char* rec = pool + t * Q::kBytes;
-    const float2 pp = ld_nc_f2(rec + Q::kParamOff + 8 * (j / Q::kVecsPerGroup));
+    const float2 pp = __ldg(params + t * Q::kGroups + j / Q::kVecsPerGroup);
     dequant_vec<BITS>(ld_nc_v4(reinterpret_cast<const uint4*>(rec) + j), pp.x, pp.y,
                       dst + t * (D / 4) + j * Q::kOutVecs);
   }

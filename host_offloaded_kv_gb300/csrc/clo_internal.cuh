@@ -2,6 +2,8 @@
 //
 // Data layout (all per context; unit u = (l * B + b) * Hkv + h):
 //   host pool (pinned, device-mapped)  bf16 [U][Nmax][K(d) | V(d)]  record = 4*d bytes
+//                                      (quantised: [U][Nmax][K codes | V codes], d*bits/4 bytes)
+//   qparams    (HBM, quantised only)   float2 [U][Nmax][2d/64]      (scale, min) per group
 //   codes      (HBM)                   uint4 [U][Nmax]               128-bit key codes
 //   qcodes     (HBM)                   uint4 [L][B][Hq]              query codes of the step
 //   qcache     (HBM)                   bf16 [U][G*d]                 query at the last refresh
@@ -65,7 +67,8 @@ struct DevState {
   int32_t* idx;                 // [U][kmax]
   uint16_t* slots;              // [U][kmax][2d]
   uint16_t* resident;           // [L][B][P][Nmax][2d]
-  const uint16_t* pool;         // device view of the host pool [U][Nmax][2d]
+  const uint16_t* pool;         // device view of the host pool [U][Nmax][record]
+  float2* qparams;              // quantised pool: [U][Nmax][2d/64] (scale, min) per group (HBM), else null
   unsigned long long* step_ctr; // [C_NUM][kCtrLanes] this step (summed by the host)
   unsigned long long* total_ctr;// [C_NUM][kCtrLanes] since init
   uint32_t* err;                // error word
@@ -242,24 +245,20 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-__device__ __forceinline__ float2 ld_nc_f2(const void* p) {
-  float2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-  return v;
-}
-
 // ---- quantised host records ---------------------------------------------------------------
-// Record of one token and kv head: [K codes | V codes | (scale, min) fp32 per 64-channel
-// group, K groups then V groups]; value i of a row sits in 32-bit word i / (32 / BITS)
-// at bit BITS * (i % (32 / BITS)).  One 16-byte code vector holds 128 / BITS values of
-// one group.
+// Record of one token and kv head in the host pool: [K codes | V codes]; value i of a row
+// sits in 32-bit word i / (32 / BITS) at bit BITS * (i % (32 / BITS)).  One 16-byte code
+// vector holds 128 / BITS values of one 64-channel group.  The groups' (scale, min) pairs
+// stay in HBM (DevState::qparams, K groups then V groups per token), so a record is a
+// whole number of 64-byte lines (d = 128: 128 bytes at 4 bits, 64 at 2 bits): records of
+// other sizes moved 10-15 % fewer useful bytes per second over the host link.
 template <int D, int BITS>
 struct QRec {
   static constexpr int kCodeVecs = 2 * D * BITS / 128;  // 16-byte code vectors per record
   static constexpr int kVecsPerGroup = BITS / 2;          // 64 values per group
   static constexpr int kOutVecs = 16 / BITS;              // bf16 uint4 per code vector
-  static constexpr int kParamOff = kCodeVecs * 16;
-  static constexpr int kBytes = kParamOff + (2 * D / 64) * 8;
+  static constexpr int kBytes = kCodeVecs * 16;
+  static constexpr int kGroups = 2 * D / 64;              // (scale, min) pairs per token
 };
 
 // Dequantises one 16-byte code vector: value = bf16(fma(q, scale, mn)).

@@ -109,12 +109,14 @@ typedef struct clo_config {
   double tau_ema;          /* weight of the newest step, in (0, 1]; default 1/16 */
   /* storage of the host pool ([KVO] section on quantised offloading: low-bit KV
    * crosses the link and is dequantised on the GPU): 16 (bf16, default; 0 means
-   * 16), 4 or 2 bits per value.  Quantised records: per token and per K or V row,
+   * 16), 4 or 2 bits per value.  Quantisation: per token and per K or V row,
    * groups of 64 channels, each with an fp32 scale = (max - min) / (2^bits - 1) and
    * fp32 min (+0 for a zero minimum); code q = clamp(rint((x - min) / scale), 0, 2^bits - 1) (0 if scale
    * is 0); the GPU sees bf16(fma(q, scale, min)) in the cache slots and resident
-   * copies.  Key hash codes come from the keys as appended.  Record bytes per token
-   * and kv head: 4 d (bf16), d + d/4 (4 bits), d/2 + d/4 (2 bits). */
+   * copies.  Key hash codes come from the keys as appended.  The host pool holds the
+   * codes; the groups' (scale, min) pairs stay in HBM (8 bytes per group: 2 d / 64
+   * groups per token and kv head).  Host record bytes per token and kv head (the bytes
+   * a fetch moves over the link): 4 d (bf16), d (4 bits), d / 2 (2 bits). */
   int32_t kv_bits;
 } clo_config;
 

@@ -280,9 +280,10 @@ void orc_kv_roundtrip(const uint16_t* x, int64_t n_values, int bits, uint16_t* y
   }
 }
 
-/* Bytes of one token's quantised K|V record of one kv head: the codes of both
- * rows and an (fp32 scale, fp32 min) pair per group; 4 d bytes (bf16) for bits 16. */
+/* Host-pool bytes of one token's K|V record of one kv head, the bytes a fetch moves
+ * over the host link: 4 d (bf16), or the codes of both rows for bits < 16 (the
+ * groups' fp32 scale and min stay in GPU memory). */
 int64_t orc_kv_record_bytes(int64_t d, int bits) {
   if (bits >= 16) return 4 * d;
-  return 2 * d * bits / 8 + (2 * d / 64) * 8;
+  return 2 * d * bits / 8;
 }

@@ -25,7 +25,7 @@ def test_int4_pool_fixed_tau():
         for t in range(5):
             ls.step(per_layer=(t == 3))
         assert sum(r["miss"] for r in ls.log) > 0 and sum(r["hit"] for r in ls.log) > 0
-        assert orc.kv_record_bytes(128, 4) == 160
+        assert orc.kv_record_bytes(128, 4) == 128
     finally:
         ls.close()
 

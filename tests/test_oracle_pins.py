@@ -420,13 +420,14 @@ def test_adaptive_tau_closed_form_converges_to_one():
 
 # ---- quantised host KV -----------------------------------------------------------------
 def test_kv_record_bytes_worked_values():
-    # one token's K|V record of one kv head: codes of 2 d values at b bits plus one
-    # (fp32 scale, fp32 min) pair per 64-channel group; d = 128: 2*128*4/8 = 128 B of
-    # codes + 4 groups * 8 B = 160 B at 4 bits, 64 + 32 = 96 B at 2 bits; bf16: 512 B
-    assert orc.kv_record_bytes(128, 4) == 160
-    assert orc.kv_record_bytes(128, 2) == 96
-    assert orc.kv_record_bytes(64, 4) == 80
-    assert orc.kv_record_bytes(64, 2) == 48
+    # host-pool bytes of one token's K|V record of one kv head (what a fetch moves over
+    # the link): the codes of 2 d values at b bits, the groups' (scale, min) pairs being
+    # kept in GPU memory; d = 128: 2*128*4/8 = 128 B at 4 bits, 64 B at 2 bits; bf16:
+    # 2 rows * 128 values * 2 B = 512 B
+    assert orc.kv_record_bytes(128, 4) == 128
+    assert orc.kv_record_bytes(128, 2) == 64
+    assert orc.kv_record_bytes(64, 4) == 64
+    assert orc.kv_record_bytes(64, 2) == 32
     assert orc.kv_record_bytes(128, 16) == 512
 
 
