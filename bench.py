@@ -457,7 +457,11 @@ def run_gb300(args, rank, world, local_rank):
     roof = kernel_roofline(hbm_bytes / steps, host_bytes / steps, fused_ms, hbm_peak, link_gbs)
     kern["fused"].update(hbm_gbs=roof["hbm_gbs"], link_gbs=roof["link_gbs"], frac_hbm=roof["frac_hbm"],
                          frac_link=roof["frac_link"], bound=roof["bound"])
-    traffic = traffic_from_profiles("k_step_fused", w.name)
+    # the capture must match the launch: a pool format or mode without its own capture
+    # under profiles/ reports no traffic
+    mode = ("" if args.kv_bits == 16 else f"_int{args.kv_bits}") + ("_layerwise" if args.layerwise else "") + \
+        ("_grow" if args.grow else "") + ("_adaptive" if args.adaptive_tau else "")
+    traffic = traffic_from_profiles("k_step_fused", w.name + mode)
     roofline = {"kernel": "k_step_fused", "bound": roof["bound"], "achieved": roof["achieved"],
                 "peak": roof["peak"], "unit": "GB/s", "frac": roof["frac"], "traffic": traffic,
                 "frac_hbm": roof["frac_hbm"], "frac_link": roof["frac_link"],
