@@ -387,7 +387,6 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.queue = z + o_queue;
     s.ready = z + o_ready;
     s.score_done = z + o_sel;
-    s.fin_done = z + o_sel + U;
     s.cnt_done = z + o_sel + 2 * U;
     s.sel_cnt = z + o_sel + 3 * U;
     c->timeline_dev = reinterpret_cast<unsigned long long*>(z + o_tl);
@@ -416,7 +415,6 @@ static clo_status init_impl(const clo_config* cfg, clo_ctx* c) {
     s.cos_cnt = nullptr;
   }
   CLO_TRY(c->dalloc(&s.sel_meta, (size_t)U * nch_max));
-  CLO_TRY(c->dalloc(&s.sel_thr, (size_t)U));
   CLO_TRY(c->dalloc(&s.total_ctr, (size_t)C_NUM * kCtrLanes));
   CLO_TRY(c->dalloc(&s.err, 1));
   CLO_TRY(c->dalloc(&s.unit_done, (size_t)U));

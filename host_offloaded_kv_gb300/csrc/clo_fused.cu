@@ -88,6 +88,7 @@ struct SelSmem {
   uint32_t hist[kCompWarps][kNBPad]; // each warp's histogram: counts of its two halves in 16-bit halves
   uint32_t tot[kNBPad];              // the unit's histogram (last chunk to arrive)
   int wc[kCompWarps][4];             // {above T, at T} of each warp's first and second half
+  int2 thr;                          // {T, count above T}
   int misc[8];
 };
 
@@ -211,8 +212,8 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
 //      coalesced), keeps the scores in shared memory and counts them in its own histogram,
 //      the two halves of its quarter in the low and high 16 bits of each bin; the chunk's
 //      histogram is added into the unit's histogram in global memory;
-//   2. the chunk that arrives last finds the unit's threshold T, the largest score with
-//      count(score >= T) >= k, and publishes T and n_gt = count(score > T);
+//   2. once every chunk's histogram is merged, each chunk finds the unit's threshold T,
+//      the largest score with count(score >= T) >= k, and n_gt = count(score > T);
 //   3. each chunk publishes its counts above and at T; from the counts of the chunks
 //      before it, a chunk knows where its indices go and how many of its ties it takes
 //      (ties go to the lowest token index: the quota k - n_gt is filled in chunk order);
@@ -376,12 +377,15 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     if (v) atomicAdd(UH + i, v);
   }
   comp_bar();  // the group's additions happen before gtid 0's release below
-  if (gtid == 0) sm.misc[0] = atom_add_acq_rel(&s.score_done[u], 1u) == (uint32_t)NC - 1u;
+  if (gtid == 0) {
+    red_release_add_u32(&s.score_done[u], 1u);
+    wait_flag(&s.score_done[u], (uint32_t)NC, s, 256);  // every chunk's histogram is merged
+  }
   comp_bar();
 
-  // 2. threshold (last chunk to arrive) or wait for it.  The last chunk also zeroes the
-  //    unit's histogram for the next step (every chunk has added to it by now).
-  if (sm.misc[0]) {
+  // 2. threshold: every chunk reads the unit's histogram and finds T itself (the chunk
+  //    that finishes its compaction last zeroes the histogram for the next step)
+  {
     constexpr int PER = (NB + kCompThreads - 1) / kCompThreads;
     uint32_t v[PER];
 #pragma unroll
@@ -392,22 +396,17 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int bin = gtid + i * kCompThreads;
-      if (bin < NB) {
-        sm.tot[bin] = v[i];
-        UH[bin] = 0u;
-      }
+      if (bin < NB) sm.tot[bin] = v[i];
     }
+    if (gtid == 0) sm.thr = make_int2(-1, 0);
     comp_bar();
-    find_threshold<NB>(sm.tot, k, &s.sel_thr[u], &sm.misc[4], gtid);
-    __threadfence();
-    comp_bar();  // the crossing thread's write happens before gtid 0's release
-    if (gtid == 0) red_release_add_u32(&s.fin_done[u], 1u);
-  }
-  if (gtid == 0) {
-    wait_flag(&s.fin_done[u], 1u, s, 256);
-    const int2 th = __ldcg(&s.sel_thr[u]);
-    sm.misc[1] = th.x < 0 ? 0 : (th.x >= NB ? NB - 1 : th.x);  // clamped: garbage only after a timeout
-    sm.misc[2] = th.y;
+    find_threshold<NB>(sm.tot, k, &sm.thr, &sm.misc[4], gtid);
+    comp_bar();
+    if (gtid == 0) {
+      const int2 th = sm.thr;
+      sm.misc[1] = th.x < 0 ? 0 : (th.x >= NB ? NB - 1 : th.x);  // clamped: garbage only after a timeout
+      sm.misc[2] = th.y;
+    }
   }
   comp_bar();
   const int T = sm.misc[1], n_gt = sm.misc[2];
@@ -502,7 +501,10 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     if (sb.a + r < sb.b) compact_round(sm.scores, sb, sb.a + r, T, take_eq, t0, out, k, s.err, lane);
   }
   comp_bar();  // the group's index writes happen before gtid 0's release
-  if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
+  if (gtid == 0) sm.misc[0] = atom_add_acq_rel(&s.sel_cnt[u], 1u) == (uint32_t)NC - 1u;
+  comp_bar();
+  if (sm.misc[0])  // every chunk has read the unit's histogram: zero it for the next step
+    for (int i = gtid; i < NB; i += kCompThreads) UH[i] = 0u;
 }
 
 // Counts of scores above and at T in tokens [a, b) of shared memory, summed over the warp

@@ -87,9 +87,7 @@ struct DevState {
   unsigned* queue;              // [2] work counters: fetch, compute (zeroed per step)
   uint32_t* unit_hist;          // [U][nbp] score histogram of each unit being selected (left zeroed by its last chunk)
   int2* sel_meta;               // [U][nch] {count above T, count at T} of each selection chunk
-  int2* sel_thr;                // [U] {threshold score T, count above T}
   uint32_t* score_done;         // [U] chunks whose histogram is merged (zeroed per step)
-  uint32_t* fin_done;           // [U] threshold published (zeroed per step)
   uint32_t* cnt_done;           // [U] chunk counts published (zeroed per step)
   uint32_t* sel_cnt;            // [U] chunks compacted (zeroed per step)
   int sel_chunk;                // tokens per selection chunk of a persistent unit
