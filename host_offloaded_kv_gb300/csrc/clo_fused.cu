@@ -85,9 +85,9 @@ struct AttSmem {
 
 struct SelSmem {
   uint16_t scores[kSelChunkMax];     // scores of the chunk's tokens
-  uint32_t hist[kCompWarps][kNBPad]; // each warp's histogram: counts of its two halves in 16-bit halves
-  uint32_t tot[kNBPad];              // the unit's histogram (last chunk to arrive)
-  int wc[kCompWarps][4];             // {above T, at T} of each warp's first and second half
+  uint32_t hist[kCompWarps][kNBPad]; // each warp's histogram of its segment
+  uint32_t tot[kNBPad];              // the unit's histogram
+  int wc[kCompWarps][2];             // {above T, at T} of each warp's segment
   int2 thr;                          // {T, count above T}
   int misc[8];
 };
@@ -96,7 +96,7 @@ struct SelSmem {
 struct SelUnitSmem {
   uint16_t scores[32768];
   uint32_t hist[kNBPad];
-  int wc[kCompWarps][4];  // {above T, at T} of each warp's first and second half
+  int wc[kCompWarps][2];  // {above T, at T} of each warp's segment
   int2 thr;               // {T, count above T}
   int misc[8];
 };
@@ -214,13 +214,14 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
 //      histogram is added into the unit's histogram in global memory;
 //   2. once every chunk's histogram is merged, each chunk finds the unit's threshold T,
 //      the largest score with count(score >= T) >= k, and n_gt = count(score > T);
-//   3. each chunk publishes its counts above and at T; from the counts of the chunks
-//      before it, a chunk knows where its indices go and how many of its ties it takes
-//      (ties go to the lowest token index: the quota k - n_gt is filled in chunk order);
-//   4. ordered compaction: each warp writes the indices of its two half-quarters as two
-//      independent streams, 4 tokens per lane per round; a lane's output position comes
-//      from ballots of the counts above and at T, so only sums are carried from round to
-//      round.
+//   3. each lane counts the scores above and at T in its own contiguous span of the
+//      warp's segment; a warp scan gives each lane the counts before its span and the
+//      chunk publishes its totals; from the totals of the chunks before it, a chunk knows
+//      where its indices go and how many of its ties it takes (ties go to the lowest token
+//      index: the quota k - n_gt is filled in chunk order);
+//   4. ordered compaction: each lane walks its span 8 tokens at a time and writes the
+//      indices of the selected ones from its own output position, with no exchange
+//      between lanes.
 // The chunks of a unit sit next to each other in the work queue and every group runs its
 // item to the end, so the waits of steps 2 and 3 only target items already running
 // (provided at least nch groups run; the host checks this).
@@ -263,59 +264,134 @@ __device__ __forceinline__ void find_threshold(const uint32_t* tot, int k, int2*
   }
 }
 
-// Ordered compaction of one stream of a warp: tokens [a, b) of the chunk (a, b multiples
-// of 4; b - a a multiple of 128 except at the chunk's end), state {off, eqb}: the next
-// output position and the number of ties (score == T) before a in the chunk.
-struct CompactStream {
-  int a, b, off, eqb;
-};
+// ---- lane spans ------------------------------------------------------------------------
+// For counting and compaction each lane owns a contiguous span of a warp's segment: 8
+// tokens times an odd number of 16-byte chunks, so that the 32 lanes' 16-byte loads fall
+// into distinct bank groups of shared memory.  Scores are compared two per 32-bit word:
+// for a word holding scores lo | hi << 16 (both <= 1024), (w + c * 0x10001) has bit 15
+// (31) set iff lo (hi) >= 0x8000 - c, with no carry between the halves.
+__device__ __forceinline__ int span_tokens(int seg) {
+  const int ch = (seg + 255) / 256;  // 16-byte chunks per lane, made odd
+  return 8 * (ch | 1);
+}
 
-__device__ __forceinline__ void compact_round(const uint16_t* scores, CompactStream& st, int base, int T,
-                                              int take_eq, int64_t t0, int32_t* out, int k, uint32_t* err,
-                                              int lane) {
-  const uint32_t lt = (1u << lane) - 1u;
-  const int t = base + 4 * lane;
-  int sc[4];
-  if (t + 3 < st.b) {
-    const uint2 v = *reinterpret_cast<const uint2*>(&scores[t]);
-    sc[0] = (int)(v.x & 0xffffu);
-    sc[1] = (int)(v.x >> 16);
-    sc[2] = (int)(v.y & 0xffffu);
-    sc[3] = (int)(v.y >> 16);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) sc[j] = t + j < st.b ? (int)scores[t + j] : -1;
-  }
-  int ngt = 0, neq = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    ngt += sc[j] > T;
-    neq += sc[j] == T;
-  }
-  const uint32_t g0 = __ballot_sync(0xffffffffu, ngt & 1), g1 = __ballot_sync(0xffffffffu, ngt & 2),
-                 g2 = __ballot_sync(0xffffffffu, ngt & 4);
-  const uint32_t e0 = __ballot_sync(0xffffffffu, neq & 1), e1 = __ballot_sync(0xffffffffu, neq & 2),
-                 e2 = __ballot_sync(0xffffffffu, neq & 4);
-  const int gt_lt = __popc(g0 & lt) + 2 * __popc(g1 & lt) + 4 * __popc(g2 & lt);
-  const int eq_lt = __popc(e0 & lt) + 2 * __popc(e1 & lt) + 4 * __popc(e2 & lt);
-  const int q = max(take_eq - st.eqb, 0);  // ties still to take at the start of the round
-  int e_run = eq_lt;                       // ties of the round before this lane's tokens
-  int pos = st.off + gt_lt + min(q, eq_lt);
+// bit 15 - i (31 - i) of the result: token 2 i (2 i + 1) of the chunk has score >= 0x8000 - c
+__device__ __forceinline__ uint32_t ge_bits(const uint4 v, uint32_t c2) {
+  const uint32_t m = 0x80008000u;
+  return ((v.x + c2) & m) | (((v.y + c2) & m) >> 1) | (((v.z + c2) & m) >> 2) | (((v.w + c2) & m) >> 3);
+}
+
+// token-order 8-bit mask (bit j = token j) from ge_bits' layout
+__device__ __forceinline__ uint32_t token_mask(uint32_t x) {
+  uint32_t lo = __brev(x << 16) & 0xfu;  // bit i = token 2 i
+  uint32_t hi = __brev(x) & 0xfu;        // bit i = token 2 i + 1
+  lo = (lo | (lo << 2)) & 0x33u;
+  lo = (lo | (lo << 1)) & 0x55u;
+  hi = (hi | (hi << 2)) & 0x33u;
+  hi = (hi | (hi << 1)) & 0x55u;
+  return lo | (hi << 1);
+}
+
+// the 8 scores of tokens [t, t + 8) as 4 words (tokens at or past b read as 0)
+__device__ __forceinline__ uint4 load_chunk(const uint16_t* scores, int t, int b) {
+  if (t + 8 <= b) return *reinterpret_cast<const uint4*>(&scores[t]);
+  uint32_t w[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const bool is_eq = sc[j] == T;
-    if (sc[j] > T || (is_eq && e_run < q)) {
+    const uint32_t l = t + 2 * j < b ? scores[t + 2 * j] : 0u;
+    const uint32_t h = t + 2 * j + 1 < b ? scores[t + 2 * j + 1] : 0u;
+    w[j] = l | (h << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// tokens of [t, t + 8) below b, in ge_bits' layout
+__device__ __forceinline__ uint32_t valid_bits(int t, int b) {
+  const int n = b - t;
+  if (n >= 8) return 0xffffffffu;
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < n) m |= (j & 1) ? (1u << (31 - j / 2)) : (1u << (15 - j / 2));
+  return m;
+}
+
+// {count above T, count at T} of tokens [lo, hi) (lo a multiple of 8)
+__device__ __forceinline__ int2 count_span(const uint16_t* scores, int lo, int hi, int T) {
+  const uint32_t cg = (uint32_t)(0x8000 - T - 1) * 0x10001u, ce = (uint32_t)(0x8000 - T) * 0x10001u;
+  int g = 0, ge = 0;
+#pragma unroll 4
+  for (int t = lo; t < hi; t += 8) {
+    const uint4 v = load_chunk(scores, t, hi);
+    const uint32_t val = valid_bits(t, hi);
+    g += __popc(ge_bits(v, cg) & val);
+    ge += __popc(ge_bits(v, ce) & val);
+  }
+  return make_int2(g, ge - g);
+}
+
+// Ordered compaction of tokens [lo, hi): tokens above T, and ties while fewer than q ties
+// precede them (er = ties before lo, counted like q), go to out[pos], out[pos + 1], ...
+// as t0 + token.
+__device__ __forceinline__ void compact_span(const uint16_t* scores, int lo, int hi, int pos, int er, int q, int T,
+                                             int64_t t0, int32_t* out, int k, uint32_t* err) {
+  const uint32_t cg = (uint32_t)(0x8000 - T - 1) * 0x10001u, ce = (uint32_t)(0x8000 - T) * 0x10001u;
+  for (int t = lo; t < hi; t += 8) {
+    const uint4 v = load_chunk(scores, t, hi);
+    const uint32_t val = valid_bits(t, hi);
+    const uint32_t gb = ge_bits(v, cg) & val, eb = ge_bits(v, ce) & val & ~gb;
+    uint32_t sel = token_mask(gb);
+    if (eb) {
+      uint32_t em = token_mask(eb);
+      const int ne = __popc(em);
+      const int room = q - er;  // ties this chunk may still take, lowest index first
+      if (room <= 0)
+        em = 0;
+      else
+        for (int drop = ne - room; drop > 0; --drop) em &= ~(0x80000000u >> __clz(em));  // drop the highest
+      sel |= em;
+      er += ne;
+    }
+    while (sel) {
+      const int j = __ffs(sel) - 1;
       if (pos < k)
         out[pos] = (int32_t)(t0 + t + j);
       else
         atomicOr(err, kErrBounds);
       ++pos;
+      sel &= sel - 1;
     }
-    e_run += is_eq;
   }
-  const int round_eq = __popc(e0) + 2 * __popc(e1) + 4 * __popc(e2);
-  st.off += __popc(g0) + 2 * __popc(g1) + 4 * __popc(g2) + min(q, round_eq);
-  st.eqb += round_eq;
+}
+
+// Counts of each lane's span of the warp's segment [w0, w1) and the warp scan over them:
+// returns the lane's span and {above, at} before it; lane 31 stores the warp's totals.
+struct LaneSpan {
+  int lo, hi, gx, ex;
+};
+
+__device__ __forceinline__ LaneSpan span_counts(const uint16_t* scores, int w0, int w1, int T, int* wc, int lane) {
+  const int e = w1 > w0 ? w1 : w0;
+  const int S = span_tokens(e - w0);
+  LaneSpan sp;
+  sp.lo = min(w0 + lane * S, e);
+  sp.hi = min(sp.lo + S, e);
+  const int2 c = count_span(scores, sp.lo, sp.hi, T);
+  const int v = c.x | (c.y << 16);  // a warp's segment holds <= 8192 tokens: 16-bit halves
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const int excl = incl - v;
+  sp.gx = excl & 0xffff;
+  sp.ex = excl >> 16;
+  if (lane == 31) {
+    wc[0] = incl & 0xffff;
+    wc[1] = incl >> 16;
+  }
+  return sp;
 }
 
 template <int G>
@@ -323,7 +399,6 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   constexpr int NB = 128 * G + 1;
   constexpr int kU = 8;                          // code loads in flight per lane
   const int WSEG = CH / kCompWarps;              // tokens per warp (CH: 1024 .. 16384), a multiple of 32 * kU
-  const int HSEG = WSEG / 2;                     // tokens per half-quarter, a multiple of 128
   const int b = (int)((u / s.Hkv) % s.B);
   const int64_t N = s.ntok[b];
   const int k = s.kcount[b];
@@ -339,7 +414,6 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   // 1. scores and histograms of this warp's segment [w0, w1)
   const int w0 = warp * WSEG;
   const int w1 = (w0 + WSEG < len) ? w0 + WSEG : len;
-  const int wmid = w0 + HSEG;  // first token of the second half
   const uint4* src = s.codes + u * s.Nmax + t0;
   constexpr int kPfRounds = 4;  // L2 prefetch of the codes this many rounds ahead
   if (lane == 0)
@@ -364,7 +438,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
       if (t < w1) {
         const int sc = score_of<G>(cv[j], qp);
         sm.scores[t] = (uint16_t)sc;
-        atomicAdd(&wh[sc], t < wmid ? 1u : 65536u);  // counts of a half fit 16 bits (<= 8192)
+        atomicAdd(&wh[sc], 1u);
       }
     }
   }
@@ -373,7 +447,7 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   for (int i = gtid; i < NB; i += kCompThreads) {
     uint32_t v = 0;
 #pragma unroll
-    for (int w = 0; w < kCompWarps; ++w) v += (sm.hist[w][i] & 0xffffu) + (sm.hist[w][i] >> 16);
+    for (int w = 0; w < kCompWarps; ++w) v += sm.hist[w][i];
     if (v) atomicAdd(UH + i, v);
   }
   comp_bar();  // the group's additions happen before gtid 0's release below
@@ -412,34 +486,17 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   const int T = sm.misc[1], n_gt = sm.misc[2];
   const int quota = k - n_gt;  // ties to take, unit-wide, lowest index first
 
-  // 3. counts of each half-quarter: {above T, at T} of the first and second half
-  {
-    int gl = 0, gh = 0;
-    for (int bin = T + 1 + lane; bin < NB; bin += 32) {
-      gl += (int)(wh[bin] & 0xffffu);
-      gh += (int)(wh[bin] >> 16);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      gl += __shfl_xor_sync(0xffffffffu, gl, o);
-      gh += __shfl_xor_sync(0xffffffffu, gh, o);
-    }
-    if (lane == 0) {
-      sm.wc[warp][0] = gl;
-      sm.wc[warp][1] = (int)(wh[T] & 0xffffu);
-      sm.wc[warp][2] = gh;
-      sm.wc[warp][3] = (int)(wh[T] >> 16);
-    }
-  }
+  // 3. each lane's counts above and at T, the warp's totals, then the chunk's
+  const LaneSpan sp = span_counts(sm.scores, w0, w1, T, sm.wc[warp], lane);
   comp_bar();
   int eq_c = 0;
 #pragma unroll
-  for (int w = 0; w < kCompWarps; ++w) eq_c += sm.wc[w][1] + sm.wc[w][3];
+  for (int w = 0; w < kCompWarps; ++w) eq_c += sm.wc[w][1];
   if (warp == 0) {
     if (lane == 0) {
       int gt_c = 0;
 #pragma unroll
-      for (int w = 0; w < kCompWarps; ++w) gt_c += sm.wc[w][0] + sm.wc[w][2];
+      for (int w = 0; w < kCompWarps; ++w) gt_c += sm.wc[w][0];
       s.sel_meta[u * NC + c] = make_int2(gt_c, eq_c);
       __threadfence();
       red_release_add_u32(&s.cnt_done[u], 1u);
@@ -472,34 +529,15 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
   int take_eq = quota - sm.misc[4];  // ties this chunk takes
   take_eq = take_eq < 0 ? 0 : (take_eq > eq_c ? eq_c : take_eq);
 
-  // 4. ordered compaction of the warp's two half-quarters as independent streams
-  CompactStream sa, sb;
-  {
-    int off = sm.misc[3], eqb = 0;
-    for (int w = 0; w <= warp; ++w)
-      for (int hf = 0; hf < 2; ++hf) {
-        if (w == warp && hf == 0) {
-          sa.off = off;
-          sa.eqb = eqb;
-        } else if (w == warp) {
-          sb.off = off;
-          sb.eqb = eqb;
-          break;
-        }
-        const int g = sm.wc[w][2 * hf], e = sm.wc[w][2 * hf + 1];
-        off += g + min(max(take_eq - eqb, 0), e);
-        eqb += e;
-      }
+  // 4. ordered compaction of each lane's span
+  int off = sm.misc[3], eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    off += sm.wc[w][0] + min(max(take_eq - eqb, 0), sm.wc[w][1]);
+    eqb += sm.wc[w][1];
   }
-  sa.a = w0;
-  sa.b = wmid < w1 ? wmid : w1;
-  sb.a = wmid;
-  sb.b = w1;
-  int32_t* out = s.idx + u * s.kmax;
-  for (int r = 0; r < HSEG; r += 128) {
-    if (sa.a + r < sa.b) compact_round(sm.scores, sa, sa.a + r, T, take_eq, t0, out, k, s.err, lane);
-    if (sb.a + r < sb.b) compact_round(sm.scores, sb, sb.a + r, T, take_eq, t0, out, k, s.err, lane);
-  }
+  const int q = max(take_eq - eqb, 0);  // ties the warp's segment takes
+  compact_span(sm.scores, sp.lo, sp.hi, off + sp.gx + min(sp.ex, q), sp.ex, q, T, t0, s.idx + u * s.kmax, k,
+               s.err);
   comp_bar();  // the group's index writes happen before gtid 0's release
   if (gtid == 0) sm.misc[0] = atom_add_acq_rel(&s.sel_cnt[u], 1u) == (uint32_t)NC - 1u;
   comp_bar();
@@ -507,38 +545,10 @@ __device__ void sel_chunk(const DevState& s, SelSmem& sm, int64_t u, int c, int 
     for (int i = gtid; i < NB; i += kCompThreads) UH[i] = 0u;
 }
 
-// Counts of scores above and at T in tokens [a, b) of shared memory, summed over the warp
-// (4 tokens per lane per round; a a multiple of 4).
-__device__ __forceinline__ int2 count_stream(const uint16_t* scores, int a, int b, int T, int lane) {
-  int gt = 0, eq = 0;
-  for (int base = a; base < b; base += 128) {
-    const int t = base + 4 * lane;
-    if (t + 3 < b) {
-      const uint2 v = *reinterpret_cast<const uint2*>(&scores[t]);
-      const int s0 = (int)(v.x & 0xffffu), s1 = (int)(v.x >> 16), s2 = (int)(v.y & 0xffffu), s3 = (int)(v.y >> 16);
-      gt += (s0 > T) + (s1 > T) + (s2 > T) + (s3 > T);
-      eq += (s0 == T) + (s1 == T) + (s2 == T) + (s3 == T);
-    } else {
-      for (int j = 0; j < 4; ++j)
-        if (t + j < b) {
-          const int sc = (int)scores[t + j];
-          gt += sc > T;
-          eq += sc == T;
-        }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, o);
-    eq += __shfl_xor_sync(0xffffffffu, eq, o);
-  }
-  return make_int2(gt, eq);
-}
-
 // ---- selection item: a whole unit (contexts up to 32K tokens) ----------------------------
 // One compute group scores all of the unit's tokens into shared memory, finds the
-// threshold T from its histogram, counts each warp's half-quarters and compacts them as
-// in a chunk: no hand-off with other groups.
+// threshold T from its histogram, counts each lane's span and compacts it as in a chunk:
+// no hand-off with other groups.
 template <int G>
 __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid) {
   constexpr int NB = 128 * G + 1;
@@ -548,7 +558,6 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
   const int k = s.kcount[b];
   const int warp = gtid >> 5, lane = gtid & 31;
   const int WSEG = (((N + kCompWarps - 1) / kCompWarps) + 255) / 256 * 256;  // tokens per warp
-  const int HSEG = WSEG / 2;
   for (int i = gtid; i < NB; i += kCompThreads) sm.hist[i] = 0;
   QPlanes<G> qp;
   load_qplanes<G>(s, u, qp);
@@ -588,45 +597,15 @@ __device__ void sel_unit(const DevState& s, SelUnitSmem& sm, int64_t u, int gtid
   comp_bar();
   const int T = sm.thr.x < 0 ? 0 : (sm.thr.x >= NB ? NB - 1 : sm.thr.x);
   const int take_eq = k - sm.thr.y;  // ties taken, lowest index first
-  const int wmid = w0 + HSEG;
-  CompactStream sa, sb;
-  sa.a = w0;
-  sa.b = wmid < w1 ? wmid : w1;
-  sb.a = wmid;
-  sb.b = w1;
-  {
-    const int2 ca = count_stream(sm.scores, sa.a, sa.b, T, lane);
-    const int2 cb = count_stream(sm.scores, sb.a, sb.b, T, lane);
-    if (lane == 0) {
-      sm.wc[warp][0] = ca.x;
-      sm.wc[warp][1] = ca.y;
-      sm.wc[warp][2] = cb.x;
-      sm.wc[warp][3] = cb.y;
-    }
-  }
+  const LaneSpan sp = span_counts(sm.scores, w0, w1, T, sm.wc[warp], lane);
   comp_bar();
-  {
-    int off = 0, eqb = 0;
-    for (int w = 0; w <= warp; ++w)
-      for (int hf = 0; hf < 2; ++hf) {
-        if (w == warp && hf == 0) {
-          sa.off = off;
-          sa.eqb = eqb;
-        } else if (w == warp) {
-          sb.off = off;
-          sb.eqb = eqb;
-          break;
-        }
-        const int g = sm.wc[w][2 * hf], e = sm.wc[w][2 * hf + 1];
-        off += g + min(max(take_eq - eqb, 0), e);
-        eqb += e;
-      }
+  int off = 0, eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    off += sm.wc[w][0] + min(max(take_eq - eqb, 0), sm.wc[w][1]);
+    eqb += sm.wc[w][1];
   }
-  int32_t* out = s.idx + u * s.kmax;
-  for (int r = 0; r < HSEG; r += 128) {
-    if (sa.a + r < sa.b) compact_round(sm.scores, sa, sa.a + r, T, take_eq, 0, out, k, s.err, lane);
-    if (sb.a + r < sb.b) compact_round(sm.scores, sb, sb.a + r, T, take_eq, 0, out, k, s.err, lane);
-  }
+  const int q = max(take_eq - eqb, 0);  // ties the warp's segment takes
+  compact_span(sm.scores, sp.lo, sp.hi, off + sp.gx + min(sp.ex, q), sp.ex, q, T, 0, s.idx + u * s.kmax, k, s.err);
   comp_bar();  // the group's index writes happen before gtid 0's release
   if (gtid == 0) red_release_add_u32(&s.sel_cnt[u], 1u);
 }
