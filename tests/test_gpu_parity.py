@@ -124,6 +124,28 @@ def test_whole_unit_selection_many_units():
     assert all(r["persist"] == 2 * 38 * 2 for r in log) and sum(r["miss"] for r in log) > 0
 
 
+@pytest.mark.parametrize("G", [3, 6, 7, 8])
+def test_group_sizes_chunked_selection(G):
+    # the bit-plane scorer at every plane count (G = 3: 2 planes, 6 and 7: 3, 8: 4, with
+    # scores up to 1024) through chunked selection: ragged lengths, one persistent head
+    pm = np.array([[1, 0]], dtype=np.uint8)
+    spec = Spec(L=1, B=2, Hq=2 * G, Hkv=2, d=64, ntok=[9001, 4099], seed=80 + G, tau=0.85, rho=(0.7, 0.98),
+                persist_mask=pm)
+    log = _run(spec, 4)
+    assert sum(r["miss"] for r in log) > 0
+
+
+def test_whole_unit_selection_largest_group():
+    # G = 8 (64/8 heads), 2 layers x 38 sequences x 8 kv heads = 608 units: the persistent
+    # units are selected whole, with scores spanning 0 .. 1024; ragged lengths
+    ntok = [2500 - 29 * b for b in range(38)]
+    pm = np.zeros((2, 8), dtype=np.uint8)
+    pm[:, [2, 7]] = 1
+    spec = Spec(L=2, B=38, Hq=64, Hkv=8, d=64, ntok=ntok, seed=88, tau=0.9, rho=(0.8, 0.99), persist_mask=pm)
+    log = _run(spec, 2)
+    assert all(r["persist"] == 2 * 38 * 2 for r in log)
+
+
 def test_cached_query_is_the_last_refresh():
     # queries turning 20, 20, 15, 15, 10 degrees per step against tau = 0.9: the reuse test
     # compares with the query of the unit's last refresh, so it misses at 40 and 70 degrees
