@@ -234,6 +234,25 @@ def kernel_roofline(hbm_bytes: float, host_bytes: float, ms: float, hbm_peak_gbs
 
 
 # ----------------------------------------------------------------------------- workload
+def step_roofline(step_bytes, hbm_bytes: float, host_bytes: float, step_ms: float, hbm_peak_gbs: float,
+                  link_peak_gbs: float) -> dict:
+    """Roofline of a run of steps that execute one after another: the ideal time is the
+    sum over the steps of each step's max(HBM bytes / HBM peak, host bytes / link peak).
+    step_bytes holds (host, HBM) bytes per timed step; hbm_bytes and host_bytes are the
+    run's totals, which give the aggregate form max(total HBM / peak, total host / peak)
+    (it understates the ideal when link-bound and HBM-bound steps alternate)."""
+    steps = len(step_bytes)
+    hbm_s, link_s = hbm_peak_gbs * 1e9, link_peak_gbs * 1e9
+    ideal_ms = sum(max(m / hbm_s, h / link_s) for h, m in step_bytes) * 1e3 / steps
+    aggregate_ms = max(hbm_bytes / hbm_s, host_bytes / link_s) * 1e3 / steps
+    return {"bound": "sum over the timed steps of max(HBM alg bytes / HBM peak, host bytes / link peak)",
+            "ideal_ms": ideal_ms, "measured_ms": step_ms, "frac": ideal_ms / step_ms,
+            "aggregate_ideal_ms": aggregate_ms, "aggregate_frac": aggregate_ms / step_ms,
+            "link_bound_steps": sum(1 for h, m in step_bytes if h / link_s >= m / hbm_s),
+            "hbm_bytes_per_step": hbm_bytes / steps, "host_bytes_per_step": host_bytes / steps,
+            "link_peak_gbs": link_peak_gbs, "hbm_peak_gbs": hbm_peak_gbs}
+
+
 def workload_from_args(args):
     from host_offloaded_kv_gb300.synth import get_workload
 
@@ -468,13 +487,6 @@ def run_gb300(args, rank, world, local_rank):
                 "hbm_bytes_per_launch": hbm_bytes / steps, "host_bytes_per_launch": host_bytes / steps,
                 "peak_source": {"hbm": f"MEASURED_PEAKS.json hbm_gbs ({hbm_src})",
                                 "host-link": "pinned H2D copy, best of 16 timed 1 GiB copies in this run"}}
-    # steps run one after another, so the roofline of the run is the sum over its steps of
-    # each step's max(HBM bytes / HBM peak, host bytes / link peak); the max of the
-    # run's averaged bytes (aggregate form) understates it when link-bound and HBM-bound
-    # steps alternate
-    per_step = [max(m / (hbm_peak * 1e9), h / (link_gbs * 1e9)) for h, m in step_bytes.tolist()]
-    step_ideal_ms = sum(per_step) * 1e3 / steps
-    aggregate_ideal_ms = max(hbm_bytes / (hbm_peak * 1e9), host_bytes / (link_gbs * 1e9)) * 1e3 / steps
     step_ms = ms_total / steps
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": W,
@@ -496,13 +508,7 @@ def run_gb300(args, rank, world, local_rank):
                       if args.grow else "")},
         "gpu_launches": steps * (2 * (L if args.layerwise else 1) + (3 if args.grow else 0)),
         "roofline": roofline,
-        "step_roofline": {"bound": "sum over the timed steps of max(HBM alg bytes / HBM peak, host bytes / link peak)",
-                          "ideal_ms": step_ideal_ms, "measured_ms": step_ms, "frac": step_ideal_ms / step_ms,
-                          "aggregate_ideal_ms": aggregate_ideal_ms, "aggregate_frac": aggregate_ideal_ms / step_ms,
-                          "link_bound_steps": sum(1 for h, m in step_bytes.tolist()
-                                                  if h / (link_gbs * 1e9) >= m / (hbm_peak * 1e9)),
-                          "hbm_bytes_per_step": hbm_bytes / steps, "host_bytes_per_step": host_bytes / steps,
-                          "link_peak_gbs": link_gbs, "hbm_peak_gbs": hbm_peak},
+        "step_roofline": step_roofline(step_bytes.tolist(), hbm_bytes, host_bytes, step_ms, hbm_peak, link_gbs),
         "kernels": kern,
         "clocks": clocks,
         "timeline_last_step": timeline,
