@@ -82,5 +82,5 @@ def test_committed_profiles_describe_the_committed_kernel():
     sys.path.insert(0, ROOT)
     import bench
 
-    for name in ("llama32k", "llama32k_int4", "llama32k_int2"):
+    for name in ("llama32k", "llama32k_int4", "llama32k_int2", "qwen512k"):
         assert bench.traffic_from_profiles("k_step_fused", name) is not None, name
